@@ -1,0 +1,411 @@
+"""Benchmark of the fused attention forward on GB300: prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one fmha_fwd over the whole workload (default: B=4, H=32, S=16384,
+D=128, fp16, no mask -- the pages' headline attention shape).  The metric is
+attention-forward TFLOPS, 4*B*H*S^2*D per step (halved under a causal mask).
+
+ours (default):
+  value     K steps with inputs resident in HBM, CUDA events on the launching
+            stream, barrier + synchronize on both sides, max over ranks.  The
+            inputs (2.15 GB) exceed the 129 MB L2, so no flush between steps.
+  e2e       the same metric through the public API with host buffers: per step
+            the pinned-host -> device copy of Q, K, V, the kernel and the
+            device -> pinned-host copy of O and LSE, all inside the timed region.
+  roofline  the attention kernel against the measured dense 16-bit tensor peak.
+  cpu_baseline  the fp64 CPU oracle on a bounded row sample of the same
+            workload on this host's cores (rank 0, N=1 only).
+reference:  the fp64 CPU oracle itself, timed the same way on bounded samples.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload (the
+(batch, head) units are independent, so per-GPU work is fixed: weak scaling);
+there is no data-path collective, only a barrier and a max of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "FMHA fwd TFLOPS at B4 H32 S16K D128 fp16; % of GB300 dense tensor peak"
+UNIT = "TFLOPS"
+KERNEL_SOURCES = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu",
+                  "fmha_api.cu"]
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def _barrier(dist, device):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def _max_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def _kernel_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "warp_specialized_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload_name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload_name)
+    if not e or e.get("kernel_sha") != _kernel_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        smi = shutil.which("nvidia-smi")
+        if smi is None or device is None:
+            return
+        ident = str(device.index)
+        try:
+            uuid = torch.cuda.get_device_properties(device).uuid
+            ident = "GPU-" + str(uuid)
+        except Exception:
+            pass
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.out = open(self.path, "w")
+        try:
+            self.proc = subprocess.Popen(
+                [smi, "-i", ident, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _row_flops(S, D, causal, rows):
+    if causal:
+        return float(sum(4.0 * (int(i) + 1) * D for i in rows))
+    return 4.0 * S * D * len(rows)
+
+
+class OracleSampler:
+    """Bounded samples of the workload for the fp64 CPU oracle: whole rows of
+    one (batch, head) slice at a time, rows spread over the sequence."""
+
+    def __init__(self, w, k_head, v_head, q_head):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.k = k_head
+        self.v = v_head
+        self.q = q_head
+        self.rng = np.random.default_rng(w.seed)
+
+    def rows(self, n):
+        return np.sort(self.rng.choice(self.w.S, size=min(n, self.w.S), replace=False))
+
+    def run(self, rows):
+        t0 = time.perf_counter()
+        self.oracle.attention_rows(self.q[rows], self.k, self.v, rows, self.w.causal,
+                                   self.w.scale)
+        dt = time.perf_counter() - t0
+        return dt, _row_flops(self.w.S, self.w.D, self.w.causal, rows)
+
+    def rows_for(self, seconds):
+        """Calibrate: how many rows take about `seconds` on this host."""
+        n = 32
+        dt, _ = self.run(self.rows(n))
+        while dt < 0.5 and n < self.w.S:
+            n = min(self.w.S, n * 4)
+            dt, _ = self.run(self.rows(n))
+        return max(1, min(self.w.S, int(n * seconds / max(dt, 1e-6))))
+
+
+def _head_inputs(w, q, k, v):
+    """One (batch, head) slice as float64 numpy (exact upcast of the stored values)."""
+    bh = (w.B * w.H) // 2
+    b, h = divmod(bh, w.H)
+    to = lambda t: t[b, h].double().cpu().numpy()  # noqa: E731
+    return to(q), to(k), to(v)
+
+
+def cpu_baseline(w, q, k, v, seconds=12.0):
+    import oracle
+    qh, kh, vh = _head_inputs(w, q, k, v)
+    smp = OracleSampler(w, kh, vh, qh)
+    n = smp.rows_for(seconds)
+    rows = smp.rows(n)
+    dt, fl = smp.run(rows)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": "%d query rows (whole rows, every visible key) of one (batch, head) slice "
+                      "of %s; %.3g GFLOP in %.2f s" % (n, w.describe(), fl / 1e9, dt),
+            "seconds": dt}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    q, k, v = synthetic.make_inputs(w, B=1, H=1)   # one head: the oracle samples rows of it
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
+    smp = OracleSampler(w, kh, vh, qh)
+    budget = 150.0  # whole run, seconds
+    per_step = max(0.5, min(6.0, budget / max(1, args.steps + args.warmup)))
+    n = smp.rows_for(per_step)
+    for _ in range(args.warmup):
+        smp.run(smp.rows(n))
+    total_t = total_f = 0.0
+    for _ in range(args.steps):
+        dt, fl = smp.run(smp.rows(n))
+        total_t += dt
+        total_f += fl
+    value = total_f / total_t / 1e12
+    sample = ("each step: %d query rows (whole rows) of one (batch, head) slice of %s"
+              % (n, w.describe()))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "dtype": w.dtype,
+            "causal": w.causal, "k_mult": w.k_mult, "scale": w.scale,
+            "layout": "BHSD contiguous, LSE fp32 (B,H,S)",
+            "l2": "inputs %.2f GB > 129 MB L2: no flush between steps"
+                  % (3 * w.B * w.H * w.S * w.D * 2 / 1e9)}
+
+
+def run_ours(args, w):
+    import warp_specialized_attention_gb300 as wsa
+    world, rank, local = _dist_env()
+    dist = _init_dist(world)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the attention path has no CPU fallback)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wsa.load_library()
+
+    q, k, v = synthetic.make_inputs_device(w, device, seed=w.seed + 7919 * rank)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        wsa.fmha_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+    torch.cuda.synchronize(device)
+    if wsa.get_device_status(stream) != wsa.FMHA_OK:
+        raise SystemExit("device status error after warm-up")
+
+    # ---- device-resident timing: one event pair per launch, on the launch stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(device) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    _barrier(dist, device)
+    torch.cuda.synchronize(device)
+    ev[0].record(stream)
+    for i in range(args.steps):
+        wsa.fmha_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    _barrier(dist, device)
+    clocks = sampler.stop() if sampler else None
+    launches = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = _max_over_ranks(dist, total_ms, device)
+    if wsa.get_device_status(stream) != wsa.FMHA_OK:
+        raise SystemExit("device status error in the timed region")
+
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops / (ms_per_step / 1e3) / 1e12
+    kernel_ms = statistics.mean(launches)
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        wsa.fmha_fwd(dq, dk, dv, o, lse, causal=w.causal, scale=w.scale, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(device)
+    _barrier(dist, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / e2e_steps
+    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))  # fp16 dense peak equals bf16's
+    traffic = _traffic(w.name)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q, k, v)
+        cpu.pop("seconds", None)
+
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic", "config": _config(w),
+        "frac_of_peak": value / world / peak,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d * world,
+                "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": "%s bf16 burst dense (fp16 nominal ratio 1)" % peak_src,
+                     "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(launches)},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synthetic.HEADLINE.name,
+                    choices=[x.name for x in synthetic.WORKLOADS])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    w = synthetic.by_name(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,100 @@
+/*
+ * wsattn.h -- C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libwsattn.so).
+ *
+ * The operation.  Attention as the pages describe it is a loop over key/value
+ * blocks with three stages per block: the first tensor-core stage S = Q K^T
+ * ("T"), a CUDA-core softmax stage ("C") and the second tensor-core stage
+ * O += P V ("U") -- "Tawa: Automatic Warp Specialization for Modern GPUs with
+ * Asynchronous References", Section III-D, Algorithm 1 (coarse-grained
+ * CUDA/Tensor Core pipeline; attention is its worked example), and the
+ * forward-attention experiments of "Optimal Software Pipelining and Warp
+ * Specialization for Tensor Core GPUs", Section 6.2 (Figs. 7 and 8: fp16,
+ * batch 4, 32 heads, head dim 128, sequence length up to 16384).  The pages
+ * name the stages but do not write the formula; this library computes the
+ * textbook definition, for every batch b, head h and query row i:
+ *
+ *     s_ij   = scale * sum_d Q[b,h,i,d] * K[b,h,j,d]
+ *     J_i    = {0 .. S-1}, or {0 .. i} when causal (key j visible iff j <= i)
+ *     O[b,h,i,:] = sum_{j in J_i} softmax_j(s_i.) * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_{j in J_i} exp(s_ij)          (natural log)
+ *
+ * with fp32 accumulation; O is stored in the input dtype, LSE in fp32.
+ */
+#ifndef WSATTN_H_
+#define WSATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  Every entry point returns one; none aborts the process. */
+typedef enum {
+  FMHA_OK = 0,
+  FMHA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, non-finite or non-positive scale */
+  FMHA_ERR_UNSUPPORTED = 2, /* valid but not implemented: D not in {64, 128}, unknown dtype */
+  FMHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (see fmha_last_cuda_error) */
+  FMHA_ERR_TIMEOUT = 4      /* a device-side wait ran past its limit; outputs are undefined */
+} fmha_status;
+
+/* Element type of Q, K, V and O. */
+typedef enum { FMHA_F16 = 0, FMHA_BF16 = 1 } fmha_dtype;
+
+/*
+ * fmha_fwd -- fused attention forward pass, O and LSE, on one GPU.
+ *
+ *   q, k, v  device pointers, each B*H*S*D elements of `dtype`, contiguous
+ *            (B, H, S, D): element (b,h,s,d) at ((b*H + h)*S + s)*D + d.
+ *            Read only.  16-byte aligned.
+ *   o        device pointer, B*H*S*D elements of `dtype`, same layout.  Written.
+ *            16-byte aligned; must not overlap q, k, v or lse.
+ *   lse      device pointer, B*H*S fp32, contiguous (B, H, S).  Written.
+ *            4-byte aligned.
+ *   B, H, S  batch, heads, sequence length (queries = keys), each >= 1;
+ *            B*H < 2^31 and ceil(S/256)*B*H < 2^31.
+ *   D        head dimension: 64 or 128 (anything else -> FMHA_ERR_UNSUPPORTED).
+ *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i.
+ *   scale    softmax scale applied to q.k, finite and > 0 (usually 1/sqrt(D)).
+ *   dtype    FMHA_F16 or FMHA_BF16.
+ *   stream   cudaStream_t (as void*) on which the kernel is enqueued; NULL is the
+ *            legacy default stream.  Must belong to the current device, which
+ *            must hold all five buffers.
+ *
+ * Ownership: the caller owns every buffer; the library allocates no device or
+ * host memory and keeps no pointer after the call returns.
+ *
+ * Behaviour: arguments are validated on the host before any CUDA call; a bad
+ * argument returns FMHA_ERR_INVALID_ARG / FMHA_ERR_UNSUPPORTED with nothing
+ * enqueued.  Otherwise one kernel is enqueued and the call returns without
+ * waiting for it (FMHA_ERR_CUDA if the launch itself failed).  A device-side
+ * timeout is reported by the next fmha_get_device_status().  Safe to call from
+ * several host threads on different streams.
+ */
+fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                     fmha_dtype dtype, void* stream);
+
+/*
+ * fmha_get_device_status -- synchronise `stream`, then report and clear the
+ * device status word of the current device.  Returns FMHA_ERR_TIMEOUT if any
+ * kernel since the previous call abandoned a wait, FMHA_ERR_CUDA if the stream
+ * reported an error, FMHA_OK otherwise.
+ */
+fmha_status fmha_get_device_status(void* stream);
+
+/* Static text for a status code. */
+const char* fmha_status_str(fmha_status status);
+
+/* Text of the CUDA error behind the calling thread's last FMHA_ERR_CUDA ("" if none). */
+const char* fmha_last_cuda_error(void);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int fmha_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSATTN_H_ */

@@ -1,0 +1,135 @@
+"""CPU-side checks of the C ABI: the libraries build, load without a GPU, export
+every function their headers declare, and reject bad arguments on the host
+before any CUDA call (so these run here, with no device)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import warp_specialized_attention_gb300 as wsa
+from warp_specialized_attention_gb300 import build as wsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wsa_build.build()
+    return wsa.load_library()
+
+
+def _declared(header):
+    text = open(os.path.join(INCLUDE, header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)) - {"defined"}
+
+
+@pytest.mark.parametrize("header,libname", [
+    ("wsattn.h", "libwsattn.so"),
+    ("wsattn_testing.h", "libwsattn.so"),
+    ("wsattn_probes.h", "libwsattn_probes.so"),
+])
+def test_every_declared_symbol_is_exported(lib, header, libname):
+    names = _declared(header)
+    assert names, "no declarations parsed from %s" % header
+    so = ctypes.CDLL(os.path.join(os.path.dirname(wsa.__file__), libname))
+    for n in sorted(names):
+        assert hasattr(so, n), "%s declares %s but %s does not export it" % (header, n, libname)
+
+
+def test_public_header_declares_the_entry_points():
+    assert {"fmha_fwd", "fmha_get_device_status", "fmha_status_str",
+            "fmha_last_cuda_error", "fmha_version"} <= _declared("wsattn.h")
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.fmha_status_str(code)
+    assert lib.fmha_version() == (0 << 16) | (1 << 8)
+
+
+# Fake, 16-byte aligned, non-overlapping "device" addresses: validation must
+# reject the call before it dereferences or passes them anywhere.
+_BASE = 1 << 40
+
+
+def _ptrs(n_bytes=1 << 30):
+    return [_BASE + i * n_bytes for i in range(5)]
+
+
+def _call(lib, ptrs=None, B=1, H=1, S=128, D=128, causal=0, scale=0.088, dtype=0):
+    q, k, v, o, lse = ptrs or _ptrs()
+    return lib.fmha_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=0), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(H=-1), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(S=0), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(D=0), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(D=96), wsa.FMHA_ERR_UNSUPPORTED),
+    (dict(D=256), wsa.FMHA_ERR_UNSUPPORTED),
+    (dict(dtype=7), wsa.FMHA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(scale=-0.1), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(B=1 << 31), wsa.FMHA_ERR_INVALID_ARG),
+    (dict(B=1 << 16, H=1 << 16), wsa.FMHA_ERR_INVALID_ARG),
+])
+def test_bad_sizes_rejected_on_host(lib, kw, expect):
+    assert _call(lib, **kw) == expect
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    p = _ptrs()
+    for i in range(5):
+        bad = list(p)
+        bad[i] = 0
+        assert _call(lib, bad) == wsa.FMHA_ERR_INVALID_ARG
+    for i in range(4):  # q, k, v, o need 16-byte alignment
+        bad = list(p)
+        bad[i] += 8
+        assert _call(lib, bad) == wsa.FMHA_ERR_INVALID_ARG
+    bad = list(p)
+    bad[4] += 2  # lse needs 4-byte alignment
+    assert _call(lib, bad) == wsa.FMHA_ERR_INVALID_ARG
+
+
+def test_overlapping_output_rejected(lib):
+    q, k, v, o, lse = _ptrs()
+    assert _call(lib, [q, k, v, q + 64, lse]) == wsa.FMHA_ERR_INVALID_ARG
+    assert _call(lib, [q, k, v, o, o + 1024]) == wsa.FMHA_ERR_INVALID_ARG
+
+
+def test_testing_hook_rejects_bad_knobs(lib):
+    q, k, v, o, lse = _ptrs()
+    args = (q, k, v, o, lse, 1, 1, 128, 128, 0, 0.088, 0, None)
+    assert lib.fmha_fwd_testing(*args, 2, 1.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 0.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 1000.0) == wsa.FMHA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    assert _call(lib) == wsa.FMHA_ERR_CUDA
+    assert lib.fmha_last_cuda_error()
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        wsa.attention(q, q, q)
+
+
+def test_no_multicast_or_trap_in_sources():
+    """The kernels use no cluster multicast, no trap and no Hopper-only MMA."""
+    csrc = os.path.join(ROOT, "warp_specialized_attention_gb300", "csrc")
+    banned = ["multicast::cluster", "__trap", "wgmma"]
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f)).read()
+        for b in banned:
+            assert b not in text, "%s uses %s" % (f, b)

@@ -1,0 +1,56 @@
+"""GPU checks of the attention kernel's building blocks on one 128-row tile:
+the S = Q K^T MMA (K-major SMEM operands from 128-byte-swizzled TMA boxes) and
+the O = P V MMA (P from Tensor Memory, V as an MN-major SMEM operand), against
+fp64 CPU products of the same 16-bit values."""
+import ctypes
+import os
+
+import pytest
+import torch
+
+import warp_specialized_attention_gb300 as wsa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def probes():
+    path = os.path.join(os.path.dirname(wsa.__file__), "libwsattn_probes.so")
+    if not os.path.exists(path):
+        pytest.fail("libwsattn_probes.so missing: run the build first")
+    lib = ctypes.CDLL(path)
+    for f in (lib.wsa_probe_qk, lib.wsa_probe_pv):
+        f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int]
+        f.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_qk_tile(probes, D, dtype):
+    g = torch.Generator().manual_seed(7 + D)
+    a = torch.randn(128, D, generator=g).to(dtype)
+    b = torch.randn(128, D, generator=g).to(dtype)
+    ref = a.double() @ b.double().T
+    c = torch.full((128, 128), float("nan"), device="cuda")
+    rc = probes.wsa_probe_qk(a.cuda().data_ptr(), b.cuda().data_ptr(), c.data_ptr(), D,
+                             int(dtype == torch.bfloat16))
+    assert rc == 0
+    err = (c.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_pv_tile(probes, D, dtype):
+    g = torch.Generator().manual_seed(11 + D)
+    p = torch.rand(128, 128, generator=g).to(dtype)
+    v = torch.randn(128, D, generator=g).to(dtype)
+    ref = p.double() @ v.double()
+    o = torch.full((128, D), float("nan"), device="cuda")
+    pd, vd = p.cuda(), v.cuda()
+    rc = probes.wsa_probe_pv(pd.data_ptr(), vd.data_ptr(), o.data_ptr(), D,
+                             int(dtype == torch.bfloat16))
+    assert rc == 0
+    err = (o.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err

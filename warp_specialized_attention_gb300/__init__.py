@@ -1,0 +1,180 @@
+"""GB300 (sm_103a) fused attention forward: O = softmax(scale * Q K^T [+ causal
+mask]) V and the per-row natural log-sum-exp, as the three-stage T/C/U loop of
+"Tawa: Automatic Warp Specialization for Modern GPUs with Asynchronous
+References", Section III-D, Algorithm 1, on one GPU.
+
+This module is a thin ctypes binding of ``libwsattn.so`` (include/wsattn.h):
+it only checks tensor metadata and marshals pointers, sizes and the stream.
+Every step of the computation runs in the library's CUDA kernel; there is no
+fallback.  If the library has not been built, importing this module succeeds
+but every call raises ``LibraryNotBuilt`` -- run
+``python -m warp_specialized_attention_gb300.build``.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
+    "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FmhaError", "LibraryNotBuilt",
+    "library_path", "load_library", "fmha_fwd", "fmha_fwd_testing", "attention",
+    "get_device_status", "status_str", "version",
+]
+
+FMHA_OK, FMHA_ERR_INVALID_ARG, FMHA_ERR_UNSUPPORTED, FMHA_ERR_CUDA, FMHA_ERR_TIMEOUT = range(5)
+FMHA_F16, FMHA_BF16 = 0, 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libwsattn.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class FmhaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = "%s: %s" % (where, status_str(status))
+        if detail:
+            msg += " (%s)" % detail
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libwsattn.so (once).  Raises LibraryNotBuilt if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise LibraryNotBuilt(
+                "libwsattn.so not found at %s; build it with "
+                "`python -m warp_specialized_attention_gb300.build`" % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        fwd_args = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                    ctypes.c_int, vp]
+        lib.fmha_fwd.argtypes = fwd_args
+        lib.fmha_fwd.restype = ctypes.c_int
+        lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double]
+        lib.fmha_fwd_testing.restype = ctypes.c_int
+        lib.fmha_get_device_status.argtypes = [vp]
+        lib.fmha_get_device_status.restype = ctypes.c_int
+        lib.fmha_status_str.argtypes = [ctypes.c_int]
+        lib.fmha_status_str.restype = ctypes.c_char_p
+        lib.fmha_last_cuda_error.argtypes = []
+        lib.fmha_last_cuda_error.restype = ctypes.c_char_p
+        lib.fmha_version.argtypes = []
+        lib.fmha_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_str(status: int) -> str:
+    try:
+        return load_library().fmha_status_str(int(status)).decode()
+    except LibraryNotBuilt:
+        return "status %d" % status
+
+
+def version() -> int:
+    return int(load_library().fmha_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FMHA_F16
+    if t.dtype == torch.bfloat16:
+        return FMHA_BF16
+    raise TypeError("q/k/v must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _check(q, k, v, o, lse):
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.shape != o.shape:
+        raise ValueError("q, k, v, o must share one (B, H, S, D) shape")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype):
+        raise TypeError("q, k, v, o must share one dtype")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("lse must be float32 of shape (B, H, S)")
+    devs = {t.device for t in (q, k, v, o, lse)}
+    if len(devs) != 1:
+        raise ValueError("all tensors must be on one device")
+
+
+def fmha_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+             stream=None) -> None:
+    """Enqueue the forward kernel: o, lse <- attention(q, k, v).
+
+    q, k, v, o: contiguous (B, H, S, D) CUDA tensors of one dtype (f16/bf16);
+    lse: contiguous (B, H, S) float32.  scale defaults to the float32 value
+    of 1/sqrt(D).  Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        st = lib.fmha_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
+                          _dtype_code(q), _stream_handle(stream))
+    if st != FMHA_OK:
+        raise FmhaError(st, "fmha_fwd", lib.fmha_last_cuda_error().decode())
+
+
+def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: int,
+                     wait_limit_s: float, stream=None) -> int:
+    """Test hook of include/wsattn_testing.h; returns the raw status code."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    B, H, S, D = q.shape
+    with torch.cuda.device(q.device):
+        return int(lib.fmha_fwd_testing(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), B, H, S, D, int(bool(causal)),
+                                        float(scale), _dtype_code(q), _stream_handle(stream),
+                                        int(inject_fault), float(wait_limit_s)))
+
+
+def get_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream; return (and clear) the device status code."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        return int(lib.fmha_get_device_status(_stream_handle(stream)))
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate O (dtype of q) and LSE (float32) with torch and run fmha_fwd."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fmha_fwd(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
+    return o, lse

@@ -1,0 +1,194 @@
+// fmha_api.cu -- the C ABI of libwsattn.so: argument validation, TMA tensor
+// maps, grid choice and launch of the warp-specialized forward kernel, plus the
+// device status word that bounded waits report into.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fmha_fwd_sm103.cuh"
+#include "fmha_launch.h"
+#include "wsattn.h"
+#include "wsattn_testing.h"
+
+namespace {
+
+// OR of wsa::kStatusTimeout* bits raised by kernels on this device since the
+// last fmha_get_device_status().
+__device__ int g_wsa_status = 0;
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+thread_local char t_last_cuda_error[256] = "";
+
+fmha_status cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s (%d)", what,
+                cudaGetErrorString(e), static_cast<int>(e));
+  return FMHA_ERR_CUDA;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver-entry-point query, so the
+// library does not link libcuda and loads on hosts without a GPU driver.
+EncodeTiledFn encode_fn(cudaError_t* err) {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && (q != cudaDriverEntryPointSuccess || f == nullptr))
+      status = cudaErrorSymbolNotFound;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  *err = status;
+  return fn;
+}
+
+// (B*H, S, D) 16-bit tensor viewed as a 3-D map, box = 64 elements (128 bytes)
+// x 128 rows x 1 head, 128-byte swizzle.  Rows past S read as zeros.
+bool encode_bhsd(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, bool bf16, int64_t BH,
+                 int64_t S, int64_t D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2),
+                                 static_cast<cuuint64_t>(S * D * 2)};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+fmha_status validate(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t S, int64_t D, float scale, int dtype) {
+  if (!q || !k || !v || !o || !lse) return FMHA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
+    return FMHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || D < 1) return FMHA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FMHA_ERR_INVALID_ARG;
+  if (dtype != FMHA_F16 && dtype != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FMHA_ERR_UNSUPPORTED;
+  const int64_t lim = (int64_t{1} << 31) - 1;
+  if (B > lim || H > lim || S > lim || B * H > lim) return FMHA_ERR_INVALID_ARG;
+  const int64_t nq = (S + 255) / 256;
+  if (nq * B * H > lim) return FMHA_ERR_INVALID_ARG;
+  const size_t n = static_cast<size_t>(B * H) * static_cast<size_t>(S) * static_cast<size_t>(D);
+  const size_t ob = n * 2, lb = static_cast<size_t>(B * H * S) * 4;
+  if (overlaps(o, ob, q, ob) || overlaps(o, ob, k, ob) || overlaps(o, ob, v, ob) ||
+      overlaps(o, ob, lse, lb) || overlaps(lse, lb, q, ob) || overlaps(lse, lb, k, ob) ||
+      overlaps(lse, lb, v, ob))
+    return FMHA_ERR_INVALID_ARG;
+  return FMHA_OK;
+}
+
+fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
+                     void* stream, int inject, uint64_t wait_limit_ns) {
+  const fmha_status vs = validate(q, k, v, o, lse, B, H, S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
+
+  cudaError_t e;
+  EncodeTiledFn enc = encode_fn(&e);
+  if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  const bool bf16 = dtype == FMHA_BF16;
+  const int64_t BH = B * H;
+  alignas(64) CUtensorMap tq, tk, tv;
+  if (!encode_bhsd(enc, &tq, q, bf16, BH, S, D) || !encode_bhsd(enc, &tk, k, bf16, BH, S, D) ||
+      !encode_bhsd(enc, &tv, v, bf16, BH, S, D))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+
+  int* status = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_wsa_status);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+
+  wsa::FwdParams prm;
+  prm.o = o;
+  prm.lse = lse;
+  prm.status = status;
+  prm.S = static_cast<int>(S);
+  prm.n_qblk = static_cast<int>((S + 255) / 256);
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.wait_limit_ns = wait_limit_ns;
+  prm.inject = inject;
+  const unsigned grid = static_cast<unsigned>(prm.n_qblk * BH);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  e = D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, prm, grid, st)
+              : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, prm, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return FMHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t S, int64_t D, int causal, float scale, fmha_dtype dtype,
+                     void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream, 0,
+                  kDefaultWaitLimitNs);
+}
+
+fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                             fmha_dtype dtype, void* stream, int inject_fault,
+                             double wait_limit_s) {
+  if (inject_fault < 0 || inject_fault > 1) return FMHA_ERR_INVALID_ARG;
+  if (!(wait_limit_s > 0.0) || wait_limit_s > 60.0) return FMHA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream,
+                  inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9));
+}
+
+fmha_status fmha_get_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_wsa_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device status");
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_wsa_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear device status");
+    return FMHA_ERR_TIMEOUT;
+  }
+  return FMHA_OK;
+}
+
+const char* fmha_status_str(fmha_status s) {
+  switch (s) {
+    case FMHA_OK: return "ok";
+    case FMHA_ERR_INVALID_ARG: return "invalid argument";
+    case FMHA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FMHA_ERR_CUDA: return "CUDA error";
+    case FMHA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* fmha_last_cuda_error(void) { return t_last_cuda_error; }
+
+int fmha_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,17 @@
+// fmha_fwd_d128.cu -- instantiations of the forward kernel for head dim 128.
+#include "fmha_fwd_sm103.cuh"
+#include "fmha_launch.h"
+
+namespace wsa {
+
+cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
+                           cudaStream_t stream) {
+  if (bf16)
+    return causal ? launch_fmha_fwd<128, true, true>(tq, tk, tv, prm, grid, stream)
+                  : launch_fmha_fwd<128, true, false>(tq, tk, tv, prm, grid, stream);
+  return causal ? launch_fmha_fwd<128, false, true>(tq, tk, tv, prm, grid, stream)
+                : launch_fmha_fwd<128, false, false>(tq, tk, tv, prm, grid, stream);
+}
+
+}  // namespace wsa

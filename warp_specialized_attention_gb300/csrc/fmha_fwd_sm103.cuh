@@ -1,0 +1,429 @@
+// fmha_fwd_sm103.cuh -- warp-specialized fused attention forward for sm_103a.
+//
+// One CTA computes 2 query tiles of 128 rows (256 rows) of one (batch, head)
+// and streams that head's keys/values in blocks of 128.  Per key block j and
+// query tile t the pages' three stages run on three kinds of unit:
+//   T : S_t = Q_t K_j^T        tcgen05.mma (SMEM x SMEM -> TMEM, fp32)
+//   C : P_t = exp2(S_t*c - m)  CUDA cores + SFU, one softmax warpgroup per tile
+//   U : O_t += P_t V_j         tcgen05.mma (TMEM x SMEM -> TMEM, fp32)
+// ("Tawa: Automatic Warp Specialization for Modern GPUs with Asynchronous
+// References", Section III-D, Algorithm 1: T_j is issued while C_{j-1} and
+// U_{j-1} are in flight).  With two query tiles the single tensor-core issuer
+// alternates between them, so one tile's softmax overlaps the other tile's
+// MMAs -- the two-consumer ping-pong that "Optimal Software Pipelining and Warp
+// Specialization for Tensor Core GPUs" rediscovers for Hopper and Blackwell
+// (Section 6.2, Figs. 7-8), built here on Tensor Memory instead of registers.
+//
+// Warp roles (320 threads, one CTA per SM):
+//   warps 0-3  softmax + epilogue, query tile 0 (TMEM lanes 0-127)
+//   warps 4-7  softmax + epilogue, query tile 1
+//   warp  8    TMEM allocator and the single-thread tcgen05.mma issuer
+//   warp  9    TMA producer: Q once, then K_j / V_j through an SMEM ring
+// The variable-latency TMA loads sit on their own warp and nothing blocking
+// shares a warp with the MMA issuer (the warp-specialization rules of the Twill
+// page, "core method": variable-latency ops on a dedicated warp, no blocking
+// wait beside interruptible ops).
+//
+// Synchronisation is the aref channel of the Tawa page (Section III-B/III-E):
+// every ring slot has a full barrier (TMA transaction bytes) and an empty
+// barrier (arrived by tcgen05.commit when the MMAs that read the slot finish);
+// use number u of a slot waits on parity (u & 1).  Between MMA issuer and
+// softmax: s_full[t] (commit after S_t), p_full[t] (128 softmax threads after P_t
+// and any O_t rescale are in TMEM), o_full[t] (commit after the last P_t V).
+//
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
+// O_1 [256+D,256+2D).  P_t (16-bit, two per column) overwrites the first 64
+// columns of S_t once the softmax has read S_t into registers.
+//
+// Online softmax with a lazy maximum: the running maximum m (in log2 units of
+// the scaled logits) is only raised when a block's maximum exceeds it by more
+// than kTau = 8, so P <= 2^8 and O_t is rescaled in TMEM only on those rare
+// blocks; the result does not depend on kTau.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace wsa {
+
+constexpr int kBM = 128;       // query rows per tile (tcgen05 M)
+constexpr int kBN = 128;       // keys per block
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
+constexpr float kTau = 8.0f;   // lazy-rescale threshold, log2 units
+constexpr uint32_t kTmemCols = 512;
+
+// Device status bits (OR-ed into the status word on an abandoned wait).
+enum : int {
+  kStatusTimeoutLoad = 1,
+  kStatusTimeoutMma = 2,
+  kStatusTimeoutSoftmax = 4,
+  kStatusTimeoutDrain = 8,
+};
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring slots
+  static constexpr int kTileBytes = kBM * D * 2;          // 128 x D 16-bit
+  static constexpr int kSlotBytes = kBN * D * 2;
+  static constexpr int kQBytes = 2 * kTileBytes;
+  static constexpr int kRingOff = kQBytes;
+  static constexpr int kCtlOff = kRingOff + kStages * kSlotBytes;
+  static constexpr int kSmemBytes = 1024 + kCtlOff + 256;  // + alignment slack + control
+  static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
+};
+
+struct Ctl {
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t mma_drain;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct FwdParams {
+  void* o;            // (B,H,S,D) 16-bit
+  float* lse;         // (B,H,S) fp32
+  int* status;        // device status word
+  int S;
+  int n_qblk;         // ceil(S / 256)
+  float scale_log2;   // scale * log2(e)
+  uint64_t wait_limit_ns;
+  int inject;         // 0 in normal use; 1 drops one softmax arrival (timeout test)
+};
+
+// K-major 128-byte-swizzled operand (Q, K): rows of 64 elements, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  return sdesc_sw128(saddr, 16, 1024);
+}
+// MN-major 128-byte-swizzled operand (V as the B operand of P V): 64-wide
+// column blocks of one slot are 128*128 bytes apart, 8-key groups 1024 apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
+  return sdesc_sw128(saddr, kBN * 128, 1024);
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_f16(BF16, kBM, kBN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+    mma_ss(d_tmem, desc_kmajor(q_smem + off), desc_kmajor(k_smem + (kk >> 2) * (kBN * 128) +
+                                                          (kk & 3) * 32),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16(BF16, kBM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
+    mma_ts(d_tmem, p_tmem + kk * 8, desc_mnmajor(v_smem + kk * 16 * 128), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms need 1024-byte aligned tiles
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+  Ctl& ctl = *reinterpret_cast<Ctl*>(smem + C::kCtlOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (head bh, 256-row query block qb)
+  const int S = p.S;
+  const int bh = blockIdx.x / p.n_qblk;
+  int qb = blockIdx.x - bh * p.n_qblk;
+  if (CAUSAL) qb = p.n_qblk - 1 - qb;  // longest rows first within a head
+  const int q0 = qb * 2 * kBM;
+  const int nkv_all = (S + kBN - 1) / kBN;
+  const int nkv0 = CAUSAL ? min(nkv_all, 2 * qb + 1) : nkv_all;
+  const int nkv1 = CAUSAL ? min(nkv_all, 2 * qb + 2) : nkv_all;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctl.s_full[t], 1);
+      mbar_init(&ctl.p_full[t], 4 * 32);
+      mbar_init(&ctl.o_full[t], 1);
+    }
+    mbar_init(&ctl.mma_drain, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&ctl.kv_full[s], 1);
+      mbar_init(&ctl.kv_empty[s], 1);
+    }
+    ctl.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+
+  const uint32_t sQ = sbase;
+  const uint32_t sRing = sbase + C::kRingOff;
+
+  if (warp == kWarpLoad) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();
+      mbar_arrive_expect_tx(&ctl.q_full, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full, cb * 64,
+                      q0 + t * kBM, bh, pol_q);
+      uint32_t it = 0;  // ring item: K_j is item 2j, V_j is item 2j+1
+      for (int j = 0; j < nkv1; ++j) {
+        bool ok = true;
+        for (int kv = 0; kv < 2; ++kv, ++it) {
+          const uint32_t slot = it % C::kStages;
+          const uint32_t use = it / C::kStages;
+          if (!mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
+                         kStatusTimeoutLoad, p.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl.kv_full[slot], C::kSlotBytes);
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_3d(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m, &ctl.kv_full[slot],
+                        cb * 64, j * kBN, bh, pol_kv);
+        }
+        if (!ok) break;
+      }
+      // Drain: every issued copy lands before the block may exit.
+      mbar_wait(&ctl.q_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+      const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
+      for (uint32_t i = first; i < it; ++i)
+        mbar_wait(&ctl.kv_full[i % C::kStages], (i / C::kStages) & 1, nullptr, p.status,
+                  kStatusTimeoutDrain, p.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS0 = tmem, tS1 = tmem + kBM;
+      const uint32_t tO0 = tmem + C::kOCol, tO1 = tmem + C::kOCol + D;
+      const uint32_t sQ0 = sQ, sQ1 = sQ + C::kTileBytes;
+      auto slot_addr = [&](uint32_t item) { return sRing + (item % C::kStages) * C::kSlotBytes; };
+      auto wait_full = [&](uint32_t item) {
+        return mbar_wait(&ctl.kv_full[item % C::kStages], (item / C::kStages) & 1, abort_flag,
+                         p.status, kStatusTimeoutMma, p.wait_limit_ns);
+      };
+      bool ok = mbar_wait(&ctl.q_full, 0, abort_flag, p.status, kStatusTimeoutMma,
+                          p.wait_limit_ns);
+      ok = ok && wait_full(0);
+      if (ok) {
+        tc_fence_after();
+        issue_qk<D, BF16>(tS0, sQ0, slot_addr(0));
+        mma_commit(&ctl.s_full[0]);
+        issue_qk<D, BF16>(tS1, sQ1, slot_addr(0));
+        mma_commit(&ctl.s_full[1]);
+        mma_commit(&ctl.kv_empty[0]);
+      }
+      for (int j = 0; ok && j < nkv1; ++j) {
+        const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
+        const bool more = j + 1 < nkv1;
+        if (!wait_full(iv)) break;
+        if (j < nkv0) {
+          if (!mbar_wait(&ctl.p_full[0], j & 1, abort_flag, p.status, kStatusTimeoutMma,
+                         p.wait_limit_ns))
+            break;
+          tc_fence_after();
+          issue_pv<D, BF16>(tO0, tS0, slot_addr(iv), j > 0);
+          if (j == nkv0 - 1) mma_commit(&ctl.o_full[0]);
+        }
+        if (more) {
+          if (!wait_full(ik)) break;
+          tc_fence_after();
+          if (j + 1 < nkv0) {
+            issue_qk<D, BF16>(tS0, sQ0, slot_addr(ik));
+            mma_commit(&ctl.s_full[0]);
+          }
+        }
+        if (!mbar_wait(&ctl.p_full[1], j & 1, abort_flag, p.status, kStatusTimeoutMma,
+                       p.wait_limit_ns))
+          break;
+        tc_fence_after();
+        issue_pv<D, BF16>(tO1, tS1, slot_addr(iv), j > 0);
+        mma_commit(&ctl.kv_empty[iv % C::kStages]);
+        if (j == nkv1 - 1) mma_commit(&ctl.o_full[1]);
+        if (more) {
+          issue_qk<D, BF16>(tS1, sQ1, slot_addr(ik));
+          mma_commit(&ctl.s_full[1]);
+          mma_commit(&ctl.kv_empty[ik % C::kStages]);
+        }
+      }
+      // Drain: all issued MMAs complete before TMEM can be released.
+      mma_commit(&ctl.mma_drain);
+      mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax tile t
+    const int t = warp >> 2;
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q0 + t * kBM + quad * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t tS = lane_base + t * kBM;
+    const uint32_t tO = lane_base + C::kOCol + t * D;
+    const int nkv = t ? nkv1 : nkv0;
+    const float cl2 = p.scale_log2;
+    // keys visible to this row: [0, lim)
+    const int lim = CAUSAL ? min(row + 1, S) : S;
+
+    float m = -INFINITY;  // running maximum, log2 units of the scaled logits
+    float l = 0.f;        // running sum of exp2(s*c - m)
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      ok = mbar_wait(&ctl.s_full[t], j & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
+                     p.wait_limit_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      float* s = reinterpret_cast<float*>(sr);
+
+      const bool masked_block = (j == nkv - 1) && (CAUSAL || (S % kBN) != 0);
+      if (masked_block) {
+        const int lim_blk = lim - j * kBN;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c >= lim_blk) s[c] = -INFINITY;
+      }
+
+      // block maximum (tree of 8 chains)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                         cl2;
+
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m = bmax;
+      } else if (bmax > m + kTau) {
+        alpha = ex2(m - bmax);
+        m = bmax;
+        rescale = true;
+      }
+      l *= alpha;
+      const float neg_m = -m;
+
+      uint32_t pk[64];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < kBN / 2; ++c) {
+        const float a = ex2(fmaf(s[2 * c], cl2, neg_m));
+        const float b = ex2(fmaf(s[2 * c + 1], cl2, neg_m));
+        ls[c & 3] += a + b;
+        pk[c] = pack2<BF16>(a, b);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tmem_st_x64(tS, pk);
+
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_t already holds every earlier block: the commit behind s_full[t]
+        // for this block was issued after the previous P_t V.
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t orr[32];
+          tmem_ld_x32(tO + ch * 32, orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st_x32(tO + ch * 32, orr);
+        }
+      }
+      tc_fence_before();
+      if (!(p.inject == 1 && t == 0 && j == 0)) mbar_arrive(&ctl.p_full[t]);
+    }
+
+    // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
+    if (ok) {
+      ok = mbar_wait(&ctl.o_full[t], 0, abort_flag, p.status, kStatusTimeoutSoftmax,
+                     p.wait_limit_ns);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool store = row < S;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((static_cast<size_t>(bh) * S + (store ? row : 0)) * D) * 2;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t orr[32];
+        tmem_ld_x32(tO + ch * 32, orr);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pkd[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv_l,
+                               __uint_as_float(orr[2 * i + 1]) * inv_l);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 64);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        }
+      }
+      if (store)
+        p.lse[static_cast<size_t>(bh) * S + row] = (m + lg2(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  // ---- teardown: every role has drained its asynchronous work
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& prm, unsigned grid, cudaStream_t stream) {
+  auto kern = fmha_fwd_kernel<D, BF16, CAUSAL>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace wsa
