@@ -33,7 +33,8 @@ def test_qk_tile(probes, D, dtype):
     b = torch.randn(128, D, generator=g).to(dtype)
     ref = a.double() @ b.double().T
     c = torch.full((128, 128), float("nan"), device="cuda")
-    rc = probes.wsa_probe_qk(a.cuda().data_ptr(), b.cuda().data_ptr(), c.data_ptr(), D,
+    ad, bd = a.cuda(), b.cuda()  # keep both alive: a temporary's memory can be reused
+    rc = probes.wsa_probe_qk(ad.data_ptr(), bd.data_ptr(), c.data_ptr(), D,
                              int(dtype == torch.bfloat16))
     assert rc == 0
     err = (c.cpu().double() - ref).abs().max().item()
