@@ -72,6 +72,31 @@ def test_small_full_compare(case):
     assert eo <= TOL_O and el <= TOL_LSE, "max err O %g LSE %g" % (eo, el)
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rising_maximum_forces_rescale(dt, causal):
+    """K is multiplied by 2 per key block, so the running maximum of many rows
+    jumps by more than the lazy-rescale threshold on block after block: this
+    drives the redo-and-rescale path of the online softmax."""
+    w = synthetic.Workload("ramp", 1, 2, 896, 128, dt, causal, 1.0, 808)
+    q, k, v = synthetic.make_inputs(w)
+    mult = (2.0 ** (torch.arange(w.S) // 128)).to(k.dtype)   # 1, 2, ..., 64 per block
+    k = (k * mult[None, None, :, None] / 4).to(k.dtype)
+    o, lse = _gpu(q, k, v, causal, w.scale)
+    o_ref, lse_ref = oracle.attention(q.double().numpy(), k.double().numpy(),
+                                      v.double().numpy(), causal, w.scale)
+    eo, el = _errors(o.cpu(), lse.cpu(), o_ref, lse_ref)
+    # These inputs are not N(0,1) (K is scaled up to 16x), so the bound comes
+    # from the arithmetic: P and O are each rounded once to the 16-bit type
+    # (unit roundoff u = 2^-11 for f16, 2^-8 for bf16), so
+    # |dO| <= u*max|V| + u*max|O| (+ fp32 and exp2 error, well under 1e-3).
+    u = 2.0 ** -8 if dt == "bf16" else 2.0 ** -11
+    tol_o = u * float(v.abs().max()) + u * float(np.abs(o_ref).max()) + 1e-3
+    print("PARITY rising-max %s %s max_err_O %.3e (bound %.3e) max_err_LSE %.3e"
+          % (dt, "causal" if causal else "full", eo, tol_o, el))
+    assert eo <= tol_o and el <= TOL_LSE, "max err O %g LSE %g" % (eo, el)
+
+
 def _sample_rows(S, rng, n_random=48):
     fixed = {0, 1, 2, 3, S - 1, S - 2, 127, 128, 129, 255, 256, 257}
     rows = {r for r in fixed if 0 <= r < S}

@@ -134,6 +134,130 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// Raw S values (fp32 bit patterns) of keys with in-block index >= lim_blk
+// become -inf (masked).
+template <int C0, int N>
+__device__ __forceinline__ void mask_keys(uint32_t* s, int lim_blk) {
+#pragma unroll
+  for (int c = 0; c < N; ++c)
+    if (C0 + c >= lim_blk) s[c] = 0xff800000u;
+}
+
+template <int N>
+__device__ __forceinline__ float row_max(const uint32_t* s) {
+  float a = __uint_as_float(s[0]), b = __uint_as_float(s[1]);
+#pragma unroll
+  for (int c = 2; c + 3 < N; c += 4) {
+    a = fmax3(a, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+    b = fmax3(b, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+  }
+  return fmaxf(fmaxf(a, b), fmaxf(__uint_as_float(s[N - 2]), __uint_as_float(s[N - 1])));
+}
+
+// P for 32 keys: p = exp2(s*c - m), rounded pairwise to 16 bits into pk; returns
+// the fp32 sum of the 32 values.
+template <bool BF16>
+__device__ __forceinline__ float exp_chunk(const uint32_t* s, uint64_t c2, uint64_t negm2,
+                                           uint32_t (&pk)[16]) {
+  uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t x = ffma2(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
+                             c2, negm2);
+    float a, b;
+    f2_unpack(x, a, b);
+    a = ex2(a);
+    b = ex2(b);
+    if (i & 1)
+      acc1 = fadd2(acc1, f2_pack(a, b));
+    else
+      acc0 = fadd2(acc0, f2_pack(a, b));
+    pk[i] = pack2<BF16>(a, b);
+  }
+  float s0, s1, s2, s3;
+  f2_unpack(acc0, s0, s1);
+  f2_unpack(acc1, s2, s3);
+  return (s0 + s1) + (s2 + s3);
+}
+
+// P for a whole block already in registers (keys 0-63 in lo, 64-127 in hi);
+// stores it over the first 64 TMEM columns of S (no wait).  Returns the sum.
+template <bool BF16>
+__device__ __forceinline__ float exp_block(const uint32_t* lo, const uint32_t* hi, float cl2,
+                                           float m, uint32_t tS) {
+  const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+  float sum = 0.f;
+  uint32_t pk[16];
+  sum += exp_chunk<BF16>(lo, c2, negm2, pk);
+  tmem_st_x16_async(tS, pk);
+  sum += exp_chunk<BF16>(lo + 32, c2, negm2, pk);
+  tmem_st_x16_async(tS + 16, pk);
+  sum += exp_chunk<BF16>(hi, c2, negm2, pk);
+  tmem_st_x16_async(tS + 32, pk);
+  sum += exp_chunk<BF16>(hi + 32, c2, negm2, pk);
+  tmem_st_x16_async(tS + 48, pk);
+  return sum;
+}
+
+// Loads keys 0-63 of S into lo and 64-127 into hi (waits).
+__device__ __forceinline__ void load_s(uint32_t tS, uint32_t (&lo)[64], uint32_t (&hi)[64]) {
+  uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[0]);
+  uint32_t(&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[32]);
+  uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
+  uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
+  tmem_ld_x32_async(tS, a);
+  tmem_ld_x32_async(tS + 32, b);
+  tmem_ld_x32_async(tS + 64, c);
+  tmem_ld_x32_async(tS + 96, d);
+  tmem_ld_wait_x32(a);
+  tmem_ld_wait_x32(b);
+  tmem_ld_wait_x32(c);
+  tmem_ld_wait_x32(d);
+}
+
+// exp_block overlapped with the TMEM loads of S in four 32-column chunks and
+// with the reduction of the block's raw maximum (returned in mx).  Keys 0-63
+// stay in lo for a possible redo; keys 64-127 pass through hi and remain
+// readable in TMEM (P only overwrites columns 0-63).
+template <bool BF16>
+__device__ __forceinline__ float exp_block_pipelined(uint32_t (&lo)[64], uint32_t (&hi)[64],
+                                                     uint32_t tS, float cl2, float m,
+                                                     bool masked, int lim_blk, float& mx) {
+  const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+  uint32_t(&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[0]);
+  uint32_t(&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[32]);
+  uint32_t(&c2r)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
+  uint32_t(&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
+  float sum = 0.f;
+  uint32_t pk[16];
+  tmem_ld_x32_async(tS, c0);
+  tmem_ld_wait_x32(c0);
+  tmem_ld_x32_async(tS + 32, c1);
+  if (masked) mask_keys<0, 32>(c0, lim_blk);
+  float mxa = row_max<32>(c0);
+  sum += exp_chunk<BF16>(c0, c2, negm2, pk);
+  tmem_st_x16_async(tS, pk);
+  tmem_ld_wait_x32(c1);
+  tmem_ld_x32_async(tS + 64, c2r);
+  if (masked) mask_keys<32, 32>(c1, lim_blk);
+  float mxb = row_max<32>(c1);
+  sum += exp_chunk<BF16>(c1, c2, negm2, pk);
+  tmem_st_x16_async(tS + 16, pk);
+  tmem_ld_wait_x32(c2r);
+  tmem_ld_x32_async(tS + 96, c3);
+  if (masked) mask_keys<64, 32>(c2r, lim_blk);
+  mxa = fmaxf(mxa, row_max<32>(c2r));
+  sum += exp_chunk<BF16>(c2r, c2, negm2, pk);
+  tmem_st_x16_async(tS + 32, pk);
+  tmem_ld_wait_x32(c3);
+  if (masked) mask_keys<96, 32>(c3, lim_blk);
+  mxb = fmaxf(mxb, row_max<32>(c3));
+  sum += exp_chunk<BF16>(c3, c2, negm2, pk);
+  tmem_st_x16_async(tS + 48, pk);
+  mx = fmaxf(mxa, mxb);
+  return sum;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -164,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.q_full, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl.s_full[t], 1);
-      mbar_init(&ctl.p_full[t], 4 * 32);
+      mbar_init(&ctl.p_full[t], 4);  // one elected arrival per softmax warp
       mbar_init(&ctl.o_full[t], 1);
     }
     mbar_init(&ctl.mma_drain, 1);
@@ -311,55 +435,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 
-      uint32_t sr[128];
-      tmem_ld_x128(tS, sr);
-      float* s = reinterpret_cast<float*>(sr);
-
       const bool masked_block = (j == nkv - 1) && (CAUSAL || (S % kBN) != 0);
-      if (masked_block) {
-        const int lim_blk = lim - j * kBN;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (c >= lim_blk) s[c] = -INFINITY;
-      }
-
-      // block maximum (tree of 8 chains)
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float bmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                         cl2;
-
-      float alpha = 1.f;
-      bool rescale = false;
+      const int lim_blk = lim - j * kBN;
+      uint32_t lo[64], hi[64];
+      float lb;            // this block's sum of P
+      float mx;            // this block's raw maximum of S
       if (j == 0) {
-        m = bmax;
-      } else if (bmax > m + kTau) {
-        alpha = ex2(m - bmax);
-        m = bmax;
-        rescale = true;
+        // First block: no running maximum yet, so take the block maximum first.
+        load_s(tS, lo, hi);
+        if (masked_block) {
+          mask_keys<0, 64>(lo, lim_blk);
+          mask_keys<64, 64>(hi, lim_blk);
+        }
+        mx = fmaxf(row_max<64>(lo), row_max<64>(hi));
+        m = mx * cl2;
+        lb = exp_block<BF16>(lo, hi, cl2, m, tS);
+      } else {
+        // Later blocks: exponentiate against the running maximum while the block
+        // maximum is still being reduced, chunk by chunk as S arrives from TMEM;
+        // the lazy-rescale rule makes this exact unless the block maximum exceeds
+        // the running one by more than kTau (handled below).
+        lb = exp_block_pipelined<BF16>(lo, hi, tS, cl2, m, masked_block, lim_blk, mx);
       }
-      l *= alpha;
-      const float neg_m = -m;
-
-      uint32_t pk[64];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float a = ex2(fmaf(s[2 * c], cl2, neg_m));
-        const float b = ex2(fmaf(s[2 * c + 1], cl2, neg_m));
-        ls[c & 3] += a + b;
-        pk[c] = pack2<BF16>(a, b);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tmem_st_x64(tS, pk);
-
+      const float bmax = mx * cl2;
+      const bool rescale = j > 0 && bmax > m + kTau;
       if (__any_sync(0xffffffffu, rescale)) {
-        // O_t already holds every earlier block: the commit behind s_full[t]
-        // for this block was issued after the previous P_t V.
+        // Rare: redo this block's P against the raised maximum and scale O_t
+        // (already complete for every earlier block: the commit behind
+        // s_full[t] was issued after the previous P_t V).  Keys 64-127 of S are
+        // still intact in TMEM; keys 0-63 are still in lo.
+        const float alpha = rescale ? ex2(m - bmax) : 1.f;
+        if (rescale) m = bmax;
+        l *= alpha;
+        tmem_st_wait();
+        {
+          uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
+          uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
+          tmem_ld_x32_async(tS + 64, c);
+          tmem_ld_x32_async(tS + 96, d);
+          tmem_ld_wait_x32(c);
+          tmem_ld_wait_x32(d);
+          if (masked_block) mask_keys<64, 64>(hi, lim_blk);
+        }
+        lb = exp_block<BF16>(lo, hi, cl2, m, tS);
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t orr[32];
@@ -369,8 +487,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_x32(tO + ch * 32, orr);
         }
       }
+      l += lb;
+      tmem_st_wait();
       tc_fence_before();
-      if (!(p.inject == 1 && t == 0 && j == 0)) mbar_arrive(&ctl.p_full[t]);
+      __syncwarp();
+      if (lane == 0 && !(p.inject == 1 && t == 0 && j == 0)) mbar_arrive(&ctl.p_full[t]);
     }
 
     // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
