@@ -28,8 +28,9 @@
 // every ring slot has a full barrier (TMA transaction bytes) and an empty
 // barrier (arrived by tcgen05.commit when the MMAs that read the slot finish);
 // use number u of a slot waits on parity (u & 1).  Between MMA issuer and
-// softmax: s_full[t] (commit after S_t), p_full[t] (128 softmax threads after P_t
-// and any O_t rescale are in TMEM), o_full[t] (commit after the last P_t V).
+// softmax: s_full[t] (commit after S_t), p_full[t] (one arrival per softmax
+// warp once P_t and any O_t rescale are in TMEM), o_full[t] (commit after the
+// last P_t V).
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
 // O_1 [256+D,256+2D).  P_t (16-bit, two per column) overwrites the first 64
@@ -38,7 +39,9 @@
 // Online softmax with a lazy maximum: the running maximum m (in log2 units of
 // the scaled logits) is only raised when a block's maximum exceeds it by more
 // than kTau = 8, so P <= 2^8 and O_t is rescaled in TMEM only on those rare
-// blocks; the result does not depend on kTau.
+// blocks; the result does not depend on kTau.  Because m is known before a
+// block's S arrives, P is computed against it as S streams out of TMEM, and the
+// block is redone in the rare case the rule raises m.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -53,6 +56,7 @@ constexpr int kThreads = 320;  // 10 warps
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr float kTau = 8.0f;   // lazy-rescale threshold, log2 units
+constexpr float kTwoPowTau = 256.0f;
 constexpr uint32_t kTmemCols = 512;
 
 // Device status bits (OR-ed into the status word on an abandoned wait).
@@ -215,14 +219,13 @@ __device__ __forceinline__ void load_s(uint32_t tS, uint32_t (&lo)[64], uint32_t
   tmem_ld_wait_x32(d);
 }
 
-// exp_block overlapped with the TMEM loads of S in four 32-column chunks and
-// with the reduction of the block's raw maximum (returned in mx).  Keys 0-63
-// stay in lo for a possible redo; keys 64-127 pass through hi and remain
-// readable in TMEM (P only overwrites columns 0-63).
+// exp_block overlapped with the TMEM loads of S in four 32-column chunks.
+// Keys 0-63 stay in lo for a possible redo; keys 64-127 pass through hi and
+// remain readable in TMEM (P only overwrites columns 0-63).
 template <bool BF16>
 __device__ __forceinline__ float exp_block_pipelined(uint32_t (&lo)[64], uint32_t (&hi)[64],
                                                      uint32_t tS, float cl2, float m,
-                                                     bool masked, int lim_blk, float& mx) {
+                                                     bool masked, int lim_blk) {
   const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
   uint32_t(&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[0]);
   uint32_t(&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[32]);
@@ -234,27 +237,22 @@ __device__ __forceinline__ float exp_block_pipelined(uint32_t (&lo)[64], uint32_
   tmem_ld_wait_x32(c0);
   tmem_ld_x32_async(tS + 32, c1);
   if (masked) mask_keys<0, 32>(c0, lim_blk);
-  float mxa = row_max<32>(c0);
   sum += exp_chunk<BF16>(c0, c2, negm2, pk);
   tmem_st_x16_async(tS, pk);
   tmem_ld_wait_x32(c1);
   tmem_ld_x32_async(tS + 64, c2r);
   if (masked) mask_keys<32, 32>(c1, lim_blk);
-  float mxb = row_max<32>(c1);
   sum += exp_chunk<BF16>(c1, c2, negm2, pk);
   tmem_st_x16_async(tS + 16, pk);
   tmem_ld_wait_x32(c2r);
   tmem_ld_x32_async(tS + 96, c3);
   if (masked) mask_keys<64, 32>(c2r, lim_blk);
-  mxa = fmaxf(mxa, row_max<32>(c2r));
   sum += exp_chunk<BF16>(c2r, c2, negm2, pk);
   tmem_st_x16_async(tS + 32, pk);
   tmem_ld_wait_x32(c3);
   if (masked) mask_keys<96, 32>(c3, lim_blk);
-  mxb = fmaxf(mxb, row_max<32>(c3));
   sum += exp_chunk<BF16>(c3, c2, negm2, pk);
   tmem_st_x16_async(tS + 48, pk);
-  mx = fmaxf(mxa, mxb);
   return sum;
 }
 
@@ -451,40 +449,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mx * cl2;
         lb = exp_block<BF16>(lo, hi, cl2, m, tS);
       } else {
-        // Later blocks: exponentiate against the running maximum while the block
-        // maximum is still being reduced, chunk by chunk as S arrives from TMEM;
-        // the lazy-rescale rule makes this exact unless the block maximum exceeds
-        // the running one by more than kTau (handled below).
-        lb = exp_block_pipelined<BF16>(lo, hi, tS, cl2, m, masked_block, lim_blk, mx);
-      }
-      const float bmax = mx * cl2;
-      const bool rescale = j > 0 && bmax > m + kTau;
-      if (__any_sync(0xffffffffu, rescale)) {
-        // Rare: redo this block's P against the raised maximum and scale O_t
-        // (already complete for every earlier block: the commit behind
-        // s_full[t] was issued after the previous P_t V).  Keys 64-127 of S are
-        // still intact in TMEM; keys 0-63 are still in lo.
-        const float alpha = rescale ? ex2(m - bmax) : 1.f;
-        if (rescale) m = bmax;
-        l *= alpha;
-        tmem_st_wait();
-        {
-          uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
-          uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
-          tmem_ld_x32_async(tS + 64, c);
-          tmem_ld_x32_async(tS + 96, d);
-          tmem_ld_wait_x32(c);
-          tmem_ld_wait_x32(d);
-          if (masked_block) mask_keys<64, 64>(hi, lim_blk);
-        }
-        lb = exp_block<BF16>(lo, hi, cl2, m, tS);
+        // Later blocks: exponentiate against the running maximum as S arrives
+        // from TMEM.  Every p is at most the block sum, so a sum <= 2^kTau
+        // proves that no logit exceeds m by more than kTau and P stands as
+        // computed.  Only a larger sum (rare once m has settled: p <= 1 while
+        // the block maximum stays below m) needs the exact block maximum.
+        lb = exp_block_pipelined<BF16>(lo, hi, tS, cl2, m, masked_block, lim_blk);
+        const bool check = lb > kTwoPowTau;
+        if (__any_sync(0xffffffffu, check)) {
+          // Keys 64-127 of S are still intact in TMEM; keys 0-63 are in lo.
+          tmem_st_wait();
+          {
+            uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
+            uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
+            tmem_ld_x32_async(tS + 64, c);
+            tmem_ld_x32_async(tS + 96, d);
+            tmem_ld_wait_x32(c);
+            tmem_ld_wait_x32(d);
+            if (masked_block) mask_keys<64, 64>(hi, lim_blk);
+          }
+          const float bmax = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
+          const bool rescale = check && bmax > m + kTau;
+          if (__any_sync(0xffffffffu, rescale)) {
+            // Redo P against the raised maximum and scale O_t (complete for
+            // every earlier block: the commit behind s_full[t] was issued after
+            // the previous P_t V).
+            const float alpha = rescale ? ex2(m - bmax) : 1.f;
+            if (rescale) m = bmax;
+            l *= alpha;
+            lb = exp_block<BF16>(lo, hi, cl2, m, tS);
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t orr[32];
-          tmem_ld_x32(tO + ch * 32, orr);
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t orr[32];
+              tmem_ld_x32(tO + ch * 32, orr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st_x32(tO + ch * 32, orr);
+              for (int i = 0; i < 32; ++i)
+                orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tmem_st_x32(tO + ch * 32, orr);
+            }
+          }
         }
       }
       l += lb;
