@@ -103,39 +103,38 @@ struct FwdParams {
   int inject;         // 0 in normal use; 1 drops one softmax arrival (timeout test)
 };
 
-// K-major 128-byte-swizzled operand (Q, K): rows of 64 elements, 8-row groups
-// 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
-  return sdesc_sw128(saddr, 16, 1024);
-}
-// MN-major 128-byte-swizzled operand (V as the B operand of P V): 64-wide
-// column blocks of one slot are 128*128 bytes apart, 8-key groups 1024 apart.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
-  return sdesc_sw128(saddr, kBN * 128, 1024);
-}
+// Shared-memory operand descriptors, 128-byte swizzle.  High half: 8-row groups
+// 1024 bytes apart.  Low half: start address plus the leading byte offset,
+// which K-major operands (Q, K: rows of 64 elements) do not use and the
+// MN-major V operand of P V uses as the distance between its 64-column blocks.
+constexpr uint32_t kDescHi = sdesc_hi(1024);
+constexpr uint32_t kLboKMajor = 16;
+constexpr uint32_t kLboV = kBN * 128;
 
+// S = Q K^T into TMEM, D/16 steps of K = 16 (32 bytes within a 128-byte row;
+// every fourth step moves to the next 16 KB column block).  Warp-collective.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
+  static_assert(kBM == kBN, "Q and K tiles share one column-block size");
   constexpr uint32_t idesc = idesc_f16(BF16, kBM, kBN, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-    mma_ss(d_tmem, desc_kmajor(q_smem + off), desc_kmajor(k_smem + (kk >> 2) * (kBN * 128) +
-                                                          (kk & 3) * 32),
-           idesc, kk > 0 ? 1u : 0u);
+    const uint32_t step = (kk >> 2) * ((kBM * 128) >> 4) + (kk & 3) * (32 >> 4);
+    mma_ss_warp(d_tmem, sdesc_join(q_lo + step, kDescHi), sdesc_join(k_lo + step, kDescHi), idesc,
+                kk > 0 ? 1u : 0u);
   }
 }
 
+// O (+)= P V: P from TMEM (16 keys = 8 columns per step), V rows 16 at a time.
+// Warp-collective.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_f16(BF16, kBM, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    // 16 keys per step: 8 TMEM columns of packed P, 16 rows (2048 bytes) of V
-    mma_ts(d_tmem, p_tmem + kk * 8, desc_mnmajor(v_smem + kk * 16 * 128), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * ((16 * 128) >> 4), kDescHi),
+                idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Raw S values (fp32 bit patterns) of keys with in-block index >= lim_blk
@@ -312,103 +311,103 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     // ================================================================ TMA producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      mbar_arrive_expect_tx(&ctl.q_full, 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_3d(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full, cb * 64,
-                      q0 + t * kBM, bh, pol_q);
-      uint32_t it = 0;  // ring item: K_j is item 2j, V_j is item 2j+1
-      for (int j = 0; j < nkv1; ++j) {
-        bool ok = true;
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const uint32_t slot = it % C::kStages;
-          const uint32_t use = it / C::kStages;
-          if (!mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
-                         kStatusTimeoutLoad, p.wait_limit_ns)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&ctl.kv_full[slot], C::kSlotBytes);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m, &ctl.kv_full[slot],
-                        cb * 64, j * kBN, bh, pol_kv);
-        }
+    // The whole warp runs the loop; one elected lane issues each copy.
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    const uint64_t pol_q = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_last();
+    mbar_arrive_expect_tx_warp(&ctl.q_full, 2 * C::kTileBytes);
+    for (int t = 0; t < 2; ++t)
+      for (int cb = 0; cb < D / 64; ++cb)
+        tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full, cb * 64,
+                         q0 + t * kBM, bh, pol_q);
+    uint32_t it = 0;  // ring item: K_j is item 2j, V_j is item 2j+1
+    bool ok = true;
+    for (int j = 0; ok && j < nkv1; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const uint32_t slot = it % C::kStages;
+        const uint32_t use = it / C::kStages;
+        ok = mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
+                       kStatusTimeoutLoad, p.wait_limit_ns);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
+        const CUtensorMap* m = kv ? &tm_v : &tm_k;
+        for (int cb = 0; cb < D / 64; ++cb)
+          tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m, &ctl.kv_full[slot],
+                           cb * 64, j * kBN, bh, pol_kv);
+        ++it;
       }
-      // Drain: every issued copy lands before the block may exit.
-      mbar_wait(&ctl.q_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
-      const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
-      for (uint32_t i = first; i < it; ++i)
-        mbar_wait(&ctl.kv_full[i % C::kStages], (i / C::kStages) & 1, nullptr, p.status,
-                  kStatusTimeoutDrain, p.wait_limit_ns);
     }
+    // Drain: every issued copy lands before the block may exit.
+    mbar_wait(&ctl.q_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
+    for (uint32_t i = first; i < it; ++i)
+      mbar_wait(&ctl.kv_full[i % C::kStages], (i / C::kStages) & 1, nullptr, p.status,
+                kStatusTimeoutDrain, p.wait_limit_ns);
     __syncwarp();
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      const uint32_t tS0 = tmem, tS1 = tmem + kBM;
-      const uint32_t tO0 = tmem + C::kOCol, tO1 = tmem + C::kOCol + D;
-      const uint32_t sQ0 = sQ, sQ1 = sQ + C::kTileBytes;
-      auto slot_addr = [&](uint32_t item) { return sRing + (item % C::kStages) * C::kSlotBytes; };
-      auto wait_full = [&](uint32_t item) {
-        return mbar_wait(&ctl.kv_full[item % C::kStages], (item / C::kStages) & 1, abort_flag,
-                         p.status, kStatusTimeoutMma, p.wait_limit_ns);
-      };
-      bool ok = mbar_wait(&ctl.q_full, 0, abort_flag, p.status, kStatusTimeoutMma,
-                          p.wait_limit_ns);
-      ok = ok && wait_full(0);
-      if (ok) {
-        tc_fence_after();
-        issue_qk<D, BF16>(tS0, sQ0, slot_addr(0));
-        mma_commit(&ctl.s_full[0]);
-        issue_qk<D, BF16>(tS1, sQ1, slot_addr(0));
-        mma_commit(&ctl.s_full[1]);
-        mma_commit(&ctl.kv_empty[0]);
-      }
-      for (int j = 0; ok && j < nkv1; ++j) {
-        const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
-        const bool more = j + 1 < nkv1;
-        if (!wait_full(iv)) break;
-        if (j < nkv0) {
-          if (!mbar_wait(&ctl.p_full[0], j & 1, abort_flag, p.status, kStatusTimeoutMma,
-                         p.wait_limit_ns))
-            break;
-          tc_fence_after();
-          issue_pv<D, BF16>(tO0, tS0, slot_addr(iv), j > 0);
-          if (j == nkv0 - 1) mma_commit(&ctl.o_full[0]);
-        }
-        if (more) {
-          if (!wait_full(ik)) break;
-          tc_fence_after();
-          if (j + 1 < nkv0) {
-            issue_qk<D, BF16>(tS0, sQ0, slot_addr(ik));
-            mma_commit(&ctl.s_full[0]);
-          }
-        }
-        if (!mbar_wait(&ctl.p_full[1], j & 1, abort_flag, p.status, kStatusTimeoutMma,
-                       p.wait_limit_ns))
-          break;
-        tc_fence_after();
-        issue_pv<D, BF16>(tO1, tS1, slot_addr(iv), j > 0);
-        mma_commit(&ctl.kv_empty[iv % C::kStages]);
-        if (j == nkv1 - 1) mma_commit(&ctl.o_full[1]);
-        if (more) {
-          issue_qk<D, BF16>(tS1, sQ1, slot_addr(ik));
-          mma_commit(&ctl.s_full[1]);
-          mma_commit(&ctl.kv_empty[ik % C::kStages]);
-        }
-      }
-      // Drain: all issued MMAs complete before TMEM can be released.
-      mma_commit(&ctl.mma_drain);
-      mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    // The whole warp runs the loop with warp-uniform operands; one elected
+    // lane issues every tcgen05.mma and tcgen05.commit.
+    const uint32_t tS0 = tmem, tS1 = tmem + kBM;
+    const uint32_t tO0 = tmem + C::kOCol, tO1 = tmem + C::kOCol + D;
+    const uint32_t q0_lo = sdesc_lo(sQ, kLboKMajor);
+    const uint32_t q1_lo = sdesc_lo(sQ + C::kTileBytes, kLboKMajor);
+    auto slot_addr = [&](uint32_t item) { return sRing + (item % C::kStages) * C::kSlotBytes; };
+    auto k_lo = [&](uint32_t item) { return sdesc_lo(slot_addr(item), kLboKMajor); };
+    auto v_lo = [&](uint32_t item) { return sdesc_lo(slot_addr(item), kLboV); };
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      const bool good =
+          mbar_wait(bar, parity, abort_flag, p.status, kStatusTimeoutMma, p.wait_limit_ns);
+      return __all_sync(0xffffffffu, good);
+    };
+    auto wait_full = [&](uint32_t item) {
+      return wait(&ctl.kv_full[item % C::kStages], (item / C::kStages) & 1);
+    };
+    bool ok = wait(&ctl.q_full, 0);
+    ok = ok && wait_full(0);
+    if (ok) {
+      tc_fence_after();
+      issue_qk<D, BF16>(tS0, q0_lo, k_lo(0));
+      mma_commit_warp(&ctl.s_full[0]);
+      issue_qk<D, BF16>(tS1, q1_lo, k_lo(0));
+      mma_commit_warp(&ctl.s_full[1]);
+      mma_commit_warp(&ctl.kv_empty[0]);
     }
+    for (int j = 0; ok && j < nkv1; ++j) {
+      const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
+      const bool more = j + 1 < nkv1;
+      if (!wait_full(iv)) break;
+      if (j < nkv0) {
+        if (!wait(&ctl.p_full[0], j & 1)) break;
+        tc_fence_after();
+        issue_pv<D, BF16>(tO0, tS0, v_lo(iv), j > 0);
+        if (j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
+      }
+      if (more) {
+        if (!wait_full(ik)) break;
+        tc_fence_after();
+        if (j + 1 < nkv0) {
+          issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
+          mma_commit_warp(&ctl.s_full[0]);
+        }
+      }
+      if (!wait(&ctl.p_full[1], j & 1)) break;
+      tc_fence_after();
+      issue_pv<D, BF16>(tO1, tS1, v_lo(iv), j > 0);
+      mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
+      if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
+      if (more) {
+        issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+        mma_commit_warp(&ctl.s_full[1]);
+        mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
+      }
+    }
+    // Drain: all issued MMAs complete before TMEM can be released.
+    mma_commit_warp(&ctl.mma_drain);
+    mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
     __syncwarp();
   } else {
     // ================================================================ softmax tile t

@@ -54,17 +54,18 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
   volatile int* ab = &ctl.abort;
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&ctl.bar_load, 2 * 128 * D * 2);
+  if (warp == 0) {  // warp-collective issue, as in the attention kernel
+    mbar_arrive_expect_tx_warp(&ctl.bar_load, 2 * 128 * D * 2);
     for (int cb = 0; cb < D / 64; ++cb) {
-      tma_load_3d(sA + cb * 128 * 128, &ta, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
-      tma_load_3d(sB + cb * 128 * 128, &tb, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
+      tma_load_3d_warp(sA + cb * 128 * 128, &ta, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
+      tma_load_3d_warp(sB + cb * 128 * 128, &tb, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
     }
-    if (mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs)) {
+    bool loaded = mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs);
+    if (__all_sync(0xffffffffu, loaded)) {
       tc_fence_after();
-      issue_qk<D, BF16>(tmem, sA, sB);
+      issue_qk<D, BF16>(tmem, sdesc_lo(sA, kLboKMajor), sdesc_lo(sB, kLboKMajor));
     }
-    mma_commit(&ctl.bar_mma);
+    mma_commit_warp(&ctl.bar_mma);
   }
   __syncwarp();
   bool ok = mbar_wait(&ctl.bar_mma, 0, nullptr, &g_probe_status, 2, kProbeWaitNs);
@@ -118,16 +119,17 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_before();
   __syncthreads();
   volatile int* ab = &ctl.abort;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {  // warp-collective issue, as in the attention kernel
     tc_fence_after();
-    mbar_arrive_expect_tx(&ctl.bar_load, 128 * D * 2);
+    mbar_arrive_expect_tx_warp(&ctl.bar_load, 128 * D * 2);
     for (int cb = 0; cb < D / 64; ++cb)
-      tma_load_3d(sV + cb * 128 * 128, &tv, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
-    if (mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs)) {
+      tma_load_3d_warp(sV + cb * 128 * 128, &tv, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
+    bool loaded = mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs);
+    if (__all_sync(0xffffffffu, loaded)) {
       tc_fence_after();
-      issue_pv<D, BF16>(tmem + 128, tmem, sV, false);
+      issue_pv<D, BF16>(tmem + 128, tmem, sdesc_lo(sV, kLboV), false);
     }
-    mma_commit(&ctl.bar_mma);
+    mma_commit_warp(&ctl.bar_mma);
   }
   __syncwarp();
   bool ok = mbar_wait(&ctl.bar_mma, 0, nullptr, &g_probe_status, 2, kProbeWaitNs);
