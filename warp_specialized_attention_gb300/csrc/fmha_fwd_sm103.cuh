@@ -28,9 +28,11 @@
 // every ring slot has a full barrier (TMA transaction bytes) and an empty
 // barrier (arrived by tcgen05.commit when the MMAs that read the slot finish);
 // use number u of a slot waits on parity (u & 1).  Between MMA issuer and
-// softmax: s_full[t] (commit after S_t), p_full[t] (one arrival per softmax
-// warp once P_t and any O_t rescale are in TMEM), o_full[t] (commit after the
-// last P_t V).
+// softmax: s_full[t] (commit after S_t), p_half[t][h] (one arrival per softmax
+// warp once P_t of key half h -- keys 64h..64h+63 -- is in TMEM, so the MMA
+// multiplies the first half into O_t while the softmax computes the second),
+// pva_done[t] (commit after that first half, awaited only by a softmax that
+// must rescale O_t mid-block), o_full[t] (commit after the last P_t V).
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
 // O_1 [256+D,256+2D).  P_t (16-bit, two per column) overwrites the first 64
@@ -83,7 +85,8 @@ struct Cfg {
 struct Ctl {
   uint64_t q_full;
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_half[2][2];   // [tile][key half]: P of keys 64h..64h+63 is in TMEM
+  uint64_t pva_done[2];    // [tile]: the P V of keys 0-63 of the current block is done
   uint64_t o_full[2];
   uint64_t mma_drain;
   uint64_t kv_full[8];
@@ -125,16 +128,25 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_
   }
 }
 
-// O (+)= P V: P from TMEM (16 keys = 8 columns per step), V rows 16 at a time.
-// Warp-collective.
+// O (+)= P V over keys [64*half, 64*half + 64): P from TMEM (16 keys = 8
+// columns per step), V rows 16 at a time.  Warp-collective.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
+                                              int half, bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16(BF16, kBM, D, true);
+#pragma unroll
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = half * 4 + k4;
+    mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * ((16 * 128) >> 4), kDescHi),
+                idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                          bool accumulate) {
-  constexpr uint32_t idesc = idesc_f16(BF16, kBM, D, true);
-#pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk)
-    mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * ((16 * 128) >> 4), kDescHi),
-                idesc, (accumulate || kk > 0) ? 1u : 0u);
+  issue_pv_half<D, BF16>(d_tmem, p_tmem, v_lo, 0, accumulate);
+  issue_pv_half<D, BF16>(d_tmem, p_tmem, v_lo, 1, true);
 }
 
 // Raw S values (fp32 bit patterns) of keys with in-block index >= lim_blk
@@ -218,40 +230,60 @@ __device__ __forceinline__ void load_s(uint32_t tS, uint32_t (&lo)[64], uint32_t
   tmem_ld_wait_x32(d);
 }
 
-// exp_block overlapped with the TMEM loads of S in four 32-column chunks.
-// Keys 0-63 stay in lo for a possible redo; keys 64-127 pass through hi and
-// remain readable in TMEM (P only overwrites columns 0-63).
+// Keys 0-63 of a block (two 32-column chunks of S into lo), exponentiated
+// against m as they arrive from TMEM; P to TMEM columns [0,32).  Starts the
+// load of keys 64-95 into hi before returning.  Returns the sum of P.
 template <bool BF16>
-__device__ __forceinline__ float exp_block_pipelined(uint32_t (&lo)[64], uint32_t (&hi)[64],
-                                                     uint32_t tS, float cl2, float m,
-                                                     bool masked, int lim_blk) {
-  const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+__device__ __forceinline__ float exp_keys_lo(uint32_t (&lo)[64], uint32_t (&hi)[64], uint32_t tS,
+                                             uint64_t c2, uint64_t negm2, bool masked,
+                                             int lim_blk) {
   uint32_t(&c0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[0]);
   uint32_t(&c1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&lo[32]);
   uint32_t(&c2r)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
-  uint32_t(&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
-  float sum = 0.f;
   uint32_t pk[16];
   tmem_ld_x32_async(tS, c0);
   tmem_ld_wait_x32(c0);
   tmem_ld_x32_async(tS + 32, c1);
   if (masked) mask_keys<0, 32>(c0, lim_blk);
-  sum += exp_chunk<BF16>(c0, c2, negm2, pk);
+  float sum = exp_chunk<BF16>(c0, c2, negm2, pk);
   tmem_st_x16_async(tS, pk);
   tmem_ld_wait_x32(c1);
   tmem_ld_x32_async(tS + 64, c2r);
   if (masked) mask_keys<32, 32>(c1, lim_blk);
   sum += exp_chunk<BF16>(c1, c2, negm2, pk);
   tmem_st_x16_async(tS + 16, pk);
+  return sum;
+}
+
+// Keys 64-127 (the first chunk's load already issued by exp_keys_lo); P to
+// TMEM columns [32,64).  Returns the sum of P.
+template <bool BF16>
+__device__ __forceinline__ float exp_keys_hi(uint32_t (&hi)[64], uint32_t tS, uint64_t c2,
+                                             uint64_t negm2, bool masked, int lim_blk) {
+  uint32_t(&c2r)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
+  uint32_t(&c3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
+  uint32_t pk[16];
   tmem_ld_wait_x32(c2r);
   tmem_ld_x32_async(tS + 96, c3);
   if (masked) mask_keys<64, 32>(c2r, lim_blk);
-  sum += exp_chunk<BF16>(c2r, c2, negm2, pk);
+  float sum = exp_chunk<BF16>(c2r, c2, negm2, pk);
   tmem_st_x16_async(tS + 32, pk);
   tmem_ld_wait_x32(c3);
   if (masked) mask_keys<96, 32>(c3, lim_blk);
   sum += exp_chunk<BF16>(c3, c2, negm2, pk);
   tmem_st_x16_async(tS + 48, pk);
+  return sum;
+}
+
+// P of 64 keys already in registers, to TMEM at tP (32 columns, no wait).
+template <bool BF16>
+__device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, float m, uint32_t tP) {
+  const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+  uint32_t pk[16];
+  float sum = exp_chunk<BF16>(s, c2, negm2, pk);
+  tmem_st_x16_async(tP, pk);
+  sum += exp_chunk<BF16>(s + 32, c2, negm2, pk);
+  tmem_st_x16_async(tP + 16, pk);
   return sum;
 }
 
@@ -285,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.q_full, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl.s_full[t], 1);
-      mbar_init(&ctl.p_full[t], 4);  // one elected arrival per softmax warp
+      mbar_init(&ctl.p_half[t][0], 4);  // one elected arrival per softmax warp
+      mbar_init(&ctl.p_half[t][1], 4);
+      mbar_init(&ctl.pva_done[t], 1);
       mbar_init(&ctl.o_full[t], 1);
     }
     mbar_init(&ctl.mma_drain, 1);
@@ -366,6 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_full = [&](uint32_t item) {
       return wait(&ctl.kv_full[item % C::kStages], (item / C::kStages) & 1);
     };
+    // O_t += P_t V in two key halves, each as soon as its P is in TMEM; the
+    // first half's completion is committed for a softmax that has to rescale
+    // O_t while computing the second half.
+    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, int j) {
+      if (!wait(&ctl.p_half[t][0], j & 1)) return false;
+      tc_fence_after();
+      issue_pv_half<D, BF16>(tO, tS, vlo, 0, j > 0);
+      mma_commit_warp(&ctl.pva_done[t]);
+      if (!wait(&ctl.p_half[t][1], j & 1)) return false;
+      tc_fence_after();
+      issue_pv_half<D, BF16>(tO, tS, vlo, 1, true);
+      return true;
+    };
     bool ok = wait(&ctl.q_full, 0);
     ok = ok && wait_full(0);
     if (ok) {
@@ -381,9 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool more = j + 1 < nkv1;
       if (!wait_full(iv)) break;
       if (j < nkv0) {
-        if (!wait(&ctl.p_full[0], j & 1)) break;
-        tc_fence_after();
-        issue_pv<D, BF16>(tO0, tS0, v_lo(iv), j > 0);
+        if (!pv_halves(0, tO0, tS0, v_lo(iv), j)) break;
         if (j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
       }
       if (more) {
@@ -394,9 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_warp(&ctl.s_full[0]);
         }
       }
-      if (!wait(&ctl.p_full[1], j & 1)) break;
-      tc_fence_after();
-      issue_pv<D, BF16>(tO1, tS1, v_lo(iv), j > 0);
+      if (!pv_halves(1, tO1, tS1, v_lo(iv), j)) break;
       mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
       if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
       if (more) {
@@ -435,8 +478,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool masked_block = (j == nkv - 1) && (CAUSAL || (S % kBN) != 0);
       const int lim_blk = lim - j * kBN;
       uint32_t lo[64], hi[64];
-      float lb;            // this block's sum of P
-      float mx;            // this block's raw maximum of S
+      // Hands one key half of P to the MMA issuer once its stores have landed.
+      auto release = [&](int half) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !(p.inject == 1 && t == 0 && j == 0 && half == 0))
+          mbar_arrive(&ctl.p_half[t][half]);
+      };
+      // O_t *= alpha for threads with alpha != 1 (all lanes take part).
+      auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t orr[32];
+          tmem_ld_x32(tO + ch * 32, orr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st_x32(tO + ch * 32, orr);
+        }
+      };
       if (j == 0) {
         // First block: no running maximum yet, so take the block maximum first.
         load_s(tS, lo, hi);
@@ -444,56 +504,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           mask_keys<0, 64>(lo, lim_blk);
           mask_keys<64, 64>(hi, lim_blk);
         }
-        mx = fmaxf(row_max<64>(lo), row_max<64>(hi));
-        m = mx * cl2;
-        lb = exp_block<BF16>(lo, hi, cl2, m, tS);
+        m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
+        l = exp_keys_regs<BF16>(lo, cl2, m, tS);
+        release(0);
+        l += exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+        release(1);
       } else {
-        // Later blocks: exponentiate against the running maximum as S arrives
-        // from TMEM.  Every p is at most the block sum, so a sum <= 2^kTau
-        // proves that no logit exceeds m by more than kTau and P stands as
-        // computed.  Only a larger sum (rare once m has settled: p <= 1 while
-        // the block maximum stays below m) needs the exact block maximum.
-        lb = exp_block_pipelined<BF16>(lo, hi, tS, cl2, m, masked_block, lim_blk);
-        const bool check = lb > kTwoPowTau;
+        // Exponentiate against the running maximum as S arrives from TMEM,
+        // one key half at a time.  Every p is at most its half's sum, so a sum
+        // <= 2^kTau proves that no logit of the half exceeds m by more than
+        // kTau and its P stands as computed; only a larger sum (rare once m has
+        // settled: p <= 1 while the block maximum stays below m) needs the
+        // exact maximum of that half.
+        uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+        float la = exp_keys_lo<BF16>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
+        bool check = la > kTwoPowTau;
         if (__any_sync(0xffffffffu, check)) {
-          // Keys 64-127 of S are still intact in TMEM; keys 0-63 are in lo.
-          tmem_st_wait();
-          {
-            uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
-            uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[32]);
-            tmem_ld_x32_async(tS + 64, c);
-            tmem_ld_x32_async(tS + 96, d);
-            tmem_ld_wait_x32(c);
-            tmem_ld_wait_x32(d);
-            if (masked_block) mask_keys<64, 64>(hi, lim_blk);
-          }
-          const float bmax = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
-          const bool rescale = check && bmax > m + kTau;
-          if (__any_sync(0xffffffffu, rescale)) {
-            // Redo P against the raised maximum and scale O_t (complete for
-            // every earlier block: the commit behind s_full[t] was issued after
-            // the previous P_t V).
-            const float alpha = rescale ? ex2(m - bmax) : 1.f;
-            if (rescale) m = bmax;
+          const float bmax = row_max<64>(lo) * cl2;
+          const bool raise = check && bmax > m + kTau;
+          if (__any_sync(0xffffffffu, raise)) {
+            // O_t holds every earlier block (the commit behind s_full[t] was
+            // issued after the previous P_t V): scale it, redo keys 0-63.
+            const float alpha = raise ? ex2(m - bmax) : 1.f;
+            if (raise) m = bmax;
             l *= alpha;
-            lb = exp_block<BF16>(lo, hi, cl2, m, tS);
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t orr[32];
-              tmem_ld_x32(tO + ch * 32, orr);
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st_x32(tO + ch * 32, orr);
-            }
+            tmem_st_wait();
+            la = exp_keys_regs<BF16>(lo, cl2, m, tS);
+            rescale_o(alpha);
+            negm2 = f2_pack(-m, -m);
           }
         }
+        l += la;
+        release(0);
+        const float lb = exp_keys_hi<BF16>(hi, tS, c2, negm2, masked_block, lim_blk);
+        check = lb > kTwoPowTau;
+        float lhi = lb;
+        if (__any_sync(0xffffffffu, check)) {
+          const float bmax = row_max<64>(hi) * cl2;
+          const bool raise = check && bmax > m + kTau;
+          if (__any_sync(0xffffffffu, raise)) {
+            // Keys 0-63 of this block are already being multiplied into O_t:
+            // wait for that half of P V, then scale O_t (it now includes them,
+            // as does l) and redo keys 64-127 against the raised maximum.
+            bool good = mbar_wait(&ctl.pva_done[t], j & 1, abort_flag, p.status,
+                                  kStatusTimeoutSoftmax, p.wait_limit_ns);
+            good = __all_sync(0xffffffffu, good);
+            if (!good) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = raise ? ex2(m - bmax) : 1.f;
+            if (raise) m = bmax;
+            l *= alpha;
+            tmem_st_wait();
+            lhi = exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+            rescale_o(alpha);
+          }
+        }
+        l += lhi;
+        release(1);
       }
-      l += lb;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0 && !(p.inject == 1 && t == 0 && j == 0)) mbar_arrive(&ctl.p_full[t]);
     }
 
     // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
