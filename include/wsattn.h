@@ -77,6 +77,36 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
                      fmha_dtype dtype, void* stream);
 
 /*
+ * fmha_fwd_host -- fmha_fwd on host-resident tensors, with the host<->device
+ * transfers overlapped with the computation.
+ *
+ *   q, k, v    host pointers, B*H*S*D elements of `dtype`, (B, H, S, D) layout.
+ *              Page-locked (pinned) memory lets the copies run asynchronously
+ *              and overlap; pageable memory works but serialises them.
+ *   o, lse     host pointers, outputs in the same layouts as fmha_fwd.
+ *   dq, dk, dv, d_o, dlse
+ *              caller-owned device staging buffers of the full sizes (same
+ *              sizes and alignment rules as fmha_fwd's q, k, v, o, lse).
+ *   n_chunks   0 for the default (8), else 1..64: the B*H (batch, head) slices
+ *              are split into this many contiguous chunks.  The host-to-device
+ *              copy of chunk c+1 and the device-to-host copy of chunk c-1 run on
+ *              two copy streams while chunk c is computed on `stream`.
+ *   Other arguments as fmha_fwd.
+ *
+ * The rows of every (batch, head) slice are independent, so the result is
+ * bit-identical to fmha_fwd on the staged device tensors.  The call returns
+ * once all work is enqueued; every copy and kernel is complete when `stream`
+ * is (synchronise `stream` before reading o and lse).  The two copy streams and
+ * a few events are created once per device and host thread and reused; no
+ * memory is allocated.  Errors as fmha_fwd (a bad pointer or size is
+ * FMHA_ERR_INVALID_ARG before anything is enqueued).
+ */
+fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
+                          int64_t H, int64_t S, int64_t D, int causal, float scale,
+                          fmha_dtype dtype, int n_chunks, void* stream);
+
+/*
  * fmha_get_device_status -- synchronise `stream`, then report and clear the
  * device status word of the current device.  Returns FMHA_ERR_TIMEOUT if any
  * kernel since the previous call abandoned a wait, FMHA_ERR_CUDA if the stream

@@ -105,6 +105,29 @@ def test_overlapping_output_rejected(lib):
     assert _call(lib, [q, k, v, o, o + 1024]) == wsa.FMHA_ERR_INVALID_ARG
 
 
+def test_host_entry_validates_before_any_cuda_call(lib):
+    host = [_BASE + (10 + i) * (1 << 30) for i in range(5)]
+    dev = _ptrs()
+    def call(h=host, d=dev, S=128, n_chunks=0):
+        return lib.fmha_fwd_host(*h, *d, 1, 2, S, 128, 0, 0.088, 0, n_chunks, None)
+    for i in range(5):
+        bad = list(host)
+        bad[i] = 0
+        assert call(h=bad) == wsa.FMHA_ERR_INVALID_ARG
+    bad = list(host)
+    bad[4] += 1  # host lse must be 4-byte aligned
+    assert call(h=bad) == wsa.FMHA_ERR_INVALID_ARG
+    bad = list(dev)
+    bad[0] += 8  # staging follows fmha_fwd's rules
+    assert call(d=bad) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(n_chunks=-1) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(n_chunks=65) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(S=0) == wsa.FMHA_ERR_INVALID_ARG
+    overl = list(host)
+    overl[3] = overl[0] + 64  # host o overlapping host q
+    assert call(h=overl) == wsa.FMHA_ERR_INVALID_ARG
+
+
 def test_testing_hook_rejects_bad_knobs(lib):
     q, k, v, o, lse = _ptrs()
     args = (q, k, v, o, lse, 1, 1, 128, 128, 0, 0.088, 0, None)

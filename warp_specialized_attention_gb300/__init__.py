@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FmhaError", "LibraryNotBuilt",
-    "library_path", "load_library", "fmha_fwd", "fmha_fwd_testing", "attention",
+    "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
     "get_device_status", "status_str", "version",
 ]
 
@@ -70,6 +70,9 @@ def load_library():
                     ctypes.c_int, vp]
         lib.fmha_fwd.argtypes = fwd_args
         lib.fmha_fwd.restype = ctypes.c_int
+        lib.fmha_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_int,
+                                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+        lib.fmha_fwd_host.restype = ctypes.c_int
         lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double]
         lib.fmha_fwd_testing.restype = ctypes.c_int
         lib.fmha_get_device_status.argtypes = [vp]
@@ -149,6 +152,33 @@ def fmha_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
                           _dtype_code(q), _stream_handle(stream))
     if st != FMHA_OK:
         raise FmhaError(st, "fmha_fwd", lib.fmha_last_cuda_error().decode())
+
+
+def fmha_fwd_host(q, k, v, o, lse, dq, dk, dv, d_o, dlse, causal: bool = False,
+                  scale: float | None = None, n_chunks: int = 0, stream=None) -> None:
+    """Enqueue attention on host tensors with overlapped transfers (C ABI
+    fmha_fwd_host): q, k, v, o (B, H, S, D) and lse (B, H, S) float32 are CPU
+    tensors (pinned for overlap); dq, dk, dv, d_o, dlse are CUDA staging
+    tensors of the same shapes.  Synchronise ``stream`` before reading o, lse.
+    """
+    lib = load_library()
+    _check(dq, dk, dv, d_o, dlse)
+    for name, t, d in (("q", q, dq), ("k", k, dk), ("v", v, dv), ("o", o, d_o), ("lse", lse, dlse)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise ValueError("%s must be a CPU tensor" % name)
+        if not t.is_contiguous() or t.shape != d.shape or t.dtype != d.dtype:
+            raise ValueError("%s must be contiguous and match its staging tensor" % name)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(dq.device):
+        st = lib.fmha_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               d_o.data_ptr(), dlse.data_ptr(), B, H, S, D, int(bool(causal)),
+                               float(scale), _dtype_code(q), int(n_chunks),
+                               _stream_handle(stream))
+    if st != FMHA_OK:
+        raise FmhaError(st, "fmha_fwd_host", lib.fmha_last_cuda_error().decode())
 
 
 def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: int,

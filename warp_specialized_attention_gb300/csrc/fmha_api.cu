@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -140,6 +141,105 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   return FMHA_OK;
 }
 
+// Per host thread and device: the two copy streams and the events that chain
+// chunks between them and the caller's stream (created on first use).
+constexpr int kMaxChunks = 64;
+constexpr int kMaxDevices = 64;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t copied[kMaxChunks], computed[kMaxChunks], entry = nullptr, done = nullptr;
+};
+thread_local HostPipe t_pipe[kMaxDevices];
+
+fmha_status host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+  HostPipe& hp = t_pipe[dev];
+  if (!hp.ready) {
+    const unsigned ev_flags = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.entry, ev_flags)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.done, ev_flags)) != cudaSuccess)
+      return cuda_fail(e, "copy stream/event creation");
+    for (int c = 0; c < kMaxChunks; ++c)
+      if ((e = cudaEventCreateWithFlags(&hp.copied[c], ev_flags)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&hp.computed[c], ev_flags)) != cudaSuccess)
+        return cuda_fail(e, "copy event creation");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FMHA_OK;
+}
+
+fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
+                          int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
+                          int n_chunks, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FMHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
+  if (n_chunks < 0 || n_chunks > kMaxChunks) return FMHA_ERR_INVALID_ARG;
+  const fmha_status vs = validate(dq, dk, dv, d_o, dlse, B, H, S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
+  const int64_t BH = B * H;
+  const size_t slice = static_cast<size_t>(S * D * 2), lslice = static_cast<size_t>(S) * 4;
+  const size_t host_bytes = static_cast<size_t>(BH) * slice;
+  if (overlaps(q, host_bytes, o, host_bytes) || overlaps(k, host_bytes, o, host_bytes) ||
+      overlaps(v, host_bytes, o, host_bytes) ||
+      overlaps(lse, static_cast<size_t>(BH) * lslice, o, host_bytes))
+    return FMHA_ERR_INVALID_ARG;
+  const int64_t chunks = std::min<int64_t>(n_chunks == 0 ? 8 : n_chunks, BH);
+
+  HostPipe* hp = nullptr;
+  const fmha_status ps = host_pipe(&hp);
+  if (ps != FMHA_OK) return ps;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // the copy streams start after everything already queued on `stream`
+  if ((e = cudaEventRecord(hp->entry, st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->h2d, hp->entry, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->d2h, hp->entry, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  auto at = [](const void* p, size_t off) {
+    return static_cast<void*>(static_cast<char*>(const_cast<void*>(p)) + off);
+  };
+  for (int64_t c = 0; c < chunks; ++c) {
+    const int64_t s0 = BH * c / chunks, s1 = BH * (c + 1) / chunks, n = s1 - s0;
+    const size_t off = static_cast<size_t>(s0) * slice, bytes = static_cast<size_t>(n) * slice;
+    const size_t loff = static_cast<size_t>(s0) * lslice, lbytes = static_cast<size_t>(n) * lslice;
+    if ((e = cudaMemcpyAsync(at(dq, off), at(q, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(at(dk, off), at(k, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(at(dv, off), at(v, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(hp->copied[c], hp->h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(st, hp->copied[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "host-to-device copy");
+    // one (batch, head) range is a B = 1, H = n problem at offset pointers
+    const fmha_status ks =
+        fwd_impl(at(dq, off), at(dk, off), at(dv, off), at(d_o, off),
+                 static_cast<float*>(at(dlse, loff)), 1, n, S, D, causal, scale, dtype, stream, 0,
+                 kDefaultWaitLimitNs);
+    if (ks != FMHA_OK) return ks;
+    if ((e = cudaEventRecord(hp->computed[c], st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(at(o, off), at(d_o, off), bytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(at(lse, loff), at(dlse, loff), lbytes, cudaMemcpyDeviceToHost,
+                             hp->d2h)) != cudaSuccess)
+      return cuda_fail(e, "device-to-host copy");
+  }
+  // `stream` completes after the last copy back
+  if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, hp->done, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  return FMHA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -159,6 +259,14 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
   if (!(wait_limit_s > 0.0) || wait_limit_s > 60.0) return FMHA_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream,
                   inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9));
+}
+
+fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
+                          int64_t H, int64_t S, int64_t D, int causal, float scale,
+                          fmha_dtype dtype, int n_chunks, void* stream) {
+  return fwd_host_impl(q, k, v, o, lse, dq, dk, dv, d_o, dlse, B, H, S, D, causal, scale,
+                       static_cast<int>(dtype), n_chunks, stream);
 }
 
 fmha_status fmha_get_device_status(void* stream) {
