@@ -1,10 +1,12 @@
 /*
  * wsattn_testing.h -- test hooks of libwsattn.so.  Not for production callers.
  *
- * The pages have no counterpart: this entry point exists so that the bounded
- * waits of the kernel (every mbarrier wait gives up after a time limit, raises
- * an abort flag for the block, drains in-flight copies and MMAs, frees Tensor
- * Memory and records a status bit) can be exercised without faulting a GPU.
+ * The pages have no counterpart: this entry point exists so that two properties
+ * of the kernel can be tested.  (1) Its bounded waits: every mbarrier wait gives
+ * up after a time limit, raises an abort flag for the block, drains in-flight
+ * copies and MMAs, frees Tensor Memory and records a status bit -- exercised
+ * here without faulting a GPU.  (2) The independence of the result from the
+ * online softmax's lazy-rescale threshold.
  */
 #ifndef WSATTN_TESTING_H_
 #define WSATTN_TESTING_H_
@@ -16,7 +18,7 @@ extern "C" {
 #endif
 
 /*
- * fmha_fwd_testing -- fmha_fwd with two extra knobs.
+ * fmha_fwd_testing -- fmha_fwd with three extra knobs.
  *
  *   inject_fault  0: none (identical to fmha_fwd).
  *                 1: the softmax warps of query tile 0 skip their first
@@ -25,6 +27,12 @@ extern "C" {
  *                    fmha_get_device_status() returns FMHA_ERR_TIMEOUT.
  *                    Outputs are undefined.
  *   wait_limit_s  per-wait time limit in seconds, in (0, 60]; fmha_fwd uses 1.
+ *   tau           lazy-rescale threshold of the online softmax in log2 units,
+ *                 in [0, 15]; fmha_fwd uses 8.  The running maximum is raised
+ *                 (and O rescaled) only when a block's maximum exceeds it by more
+ *                 than tau, so P <= 2^tau (15 keeps P inside the f16 range).  The
+ *                 result does not depend on tau; 0 gives the classic online
+ *                 softmax that rescales whenever the maximum grows.
  *
  * Other arguments, ownership and errors as fmha_fwd; an out-of-range knob is
  * FMHA_ERR_INVALID_ARG.
@@ -32,7 +40,7 @@ extern "C" {
 fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* o, float* lse,
                              int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
                              fmha_dtype dtype, void* stream, int inject_fault,
-                             double wait_limit_s);
+                             double wait_limit_s, float tau);
 
 #ifdef __cplusplus
 }

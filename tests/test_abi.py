@@ -131,9 +131,12 @@ def test_host_entry_validates_before_any_cuda_call(lib):
 def test_testing_hook_rejects_bad_knobs(lib):
     q, k, v, o, lse = _ptrs()
     args = (q, k, v, o, lse, 1, 1, 128, 128, 0, 0.088, 0, None)
-    assert lib.fmha_fwd_testing(*args, 2, 1.0) == wsa.FMHA_ERR_INVALID_ARG
-    assert lib.fmha_fwd_testing(*args, 0, 0.0) == wsa.FMHA_ERR_INVALID_ARG
-    assert lib.fmha_fwd_testing(*args, 0, 1000.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 2, 1.0, 8.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 0.0, 8.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 1000.0, 8.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 1.0, -1.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 1.0, 16.0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_testing(*args, 0, 1.0, float("nan")) == wsa.FMHA_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

@@ -162,3 +162,41 @@ def test_scale_is_applied():
                                           v.double().numpy(), False, scale)
         eo, el = _errors(o.cpu(), lse.cpu(), o_ref, lse_ref)
         assert eo <= TOL_O and el <= TOL_LSE
+
+
+@pytest.mark.parametrize("case", [
+    (1, 2, 1024, 128, "f16", False, 1.0),
+    (1, 2, 1000, 128, "bf16", True, 1.0),
+    (1, 2, 768, 64, "f16", True, 4.0),
+], ids=lambda c: "S%d-D%d-%s-%s-k%g" % (c[2], c[3], c[4], "causal" if c[5] else "full", c[6]))
+def test_result_independent_of_lazy_rescale_threshold(case):
+    """tau = 0 is the classic online softmax (rescale whenever the maximum
+    grows, which also drives the exact-maximum check on nearly every block);
+    tau = 8 is the default lazy rule; tau = 15 the largest allowed.  All must
+    match the oracle, and each other to within rounding."""
+    B, H, S, D, dt, causal, k_mult = case
+    w = synthetic.Workload("tau", B, H, S, D, dt, causal, k_mult, 9000 + S)
+    q, k, v = synthetic.make_inputs(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = oracle.attention(q.double().numpy(), k.double().numpy(),
+                                      v.double().numpy(), causal, w.scale)
+    outs = {}
+    for tau in (0.0, 8.0, 15.0):
+        o = torch.full_like(qd, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), device="cuda", dtype=torch.float32)
+        assert wsa.fmha_fwd_testing(qd, kd, vd, o, lse, causal, w.scale, 0, 1.0, tau) == wsa.FMHA_OK
+        assert wsa.get_device_status() == wsa.FMHA_OK
+        eo, el = _errors(o.cpu(), lse.cpu(), o_ref, lse_ref)
+        print("PARITY tau=%g %s max_err_O %.3e max_err_LSE %.3e" % (tau, w.describe(), eo, el))
+        assert eo <= TOL_O and el <= TOL_LSE
+        outs[tau] = (o.float(), lse)
+    # Different tau only changes which maximum P is scaled against, so the two
+    # results differ by the rounding of P and of O to the 16-bit type (unit
+    # roundoff u) on each side: at most 2u*max|V| + 2u*max|O| (+ fp32 noise).
+    u = 2.0 ** -8 if dt == "bf16" else 2.0 ** -11
+    bound = 2 * u * float(v.abs().max()) + 2 * u * float(np.abs(o_ref).max()) + 1e-4
+    for tau in (0.0, 15.0):
+        d_o = (outs[tau][0] - outs[8.0][0]).abs().max().item()
+        d_l = (outs[tau][1] - outs[8.0][1]).abs().max().item()
+        assert d_o <= bound and d_l <= 2e-5, "tau %g vs 8: dO %g (bound %g) dLSE %g" % (
+            tau, d_o, bound, d_l)

@@ -73,7 +73,7 @@ def load_library():
         lib.fmha_fwd_host.argtypes = [vp] * 10 + [i64, i64, i64, i64, ctypes.c_int,
                                                   ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
         lib.fmha_fwd_host.restype = ctypes.c_int
-        lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double]
+        lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double, ctypes.c_float]
         lib.fmha_fwd_testing.restype = ctypes.c_int
         lib.fmha_get_device_status.argtypes = [vp]
         lib.fmha_get_device_status.restype = ctypes.c_int
@@ -182,7 +182,7 @@ def fmha_fwd_host(q, k, v, o, lse, dq, dk, dv, d_o, dlse, causal: bool = False,
 
 
 def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: int,
-                     wait_limit_s: float, stream=None) -> int:
+                     wait_limit_s: float, tau: float = 8.0, stream=None) -> int:
     """Test hook of include/wsattn_testing.h; returns the raw status code."""
     lib = load_library()
     _check(q, k, v, o, lse)
@@ -191,7 +191,7 @@ def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: 
         return int(lib.fmha_fwd_testing(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                         lse.data_ptr(), B, H, S, D, int(bool(causal)),
                                         float(scale), _dtype_code(q), _stream_handle(stream),
-                                        int(inject_fault), float(wait_limit_s)))
+                                        int(inject_fault), float(wait_limit_s), float(tau)))
 
 
 def get_device_status(stream=None, device=None) -> int:

@@ -105,7 +105,8 @@ fmha_status validate(const void* q, const void* k, const void* v, void* o, float
 
 fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
-                     void* stream, int inject, uint64_t wait_limit_ns) {
+                     void* stream, int inject, uint64_t wait_limit_ns,
+                     float tau = wsa::kTauDefault) {
   const fmha_status vs = validate(q, k, v, o, lse, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
 
@@ -132,6 +133,8 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = wait_limit_ns;
   prm.inject = inject;
+  prm.tau = tau;
+  prm.two_pow_tau = std::exp2(tau);
   const unsigned grid = static_cast<unsigned>(prm.n_qblk * BH);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -254,11 +257,12 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
 fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* o, float* lse,
                              int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
                              fmha_dtype dtype, void* stream, int inject_fault,
-                             double wait_limit_s) {
+                             double wait_limit_s, float tau) {
   if (inject_fault < 0 || inject_fault > 1) return FMHA_ERR_INVALID_ARG;
   if (!(wait_limit_s > 0.0) || wait_limit_s > 60.0) return FMHA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f && tau <= 15.f)) return FMHA_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream,
-                  inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9));
+                  inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9), tau);
 }
 
 fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,

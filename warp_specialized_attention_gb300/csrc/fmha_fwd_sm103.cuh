@@ -40,8 +40,9 @@
 //
 // Online softmax with a lazy maximum: the running maximum m (in log2 units of
 // the scaled logits) is only raised when a block's maximum exceeds it by more
-// than kTau = 8, so P <= 2^8 and O_t is rescaled in TMEM only on those rare
-// blocks; the result does not depend on kTau.  Because m is known before a
+// than tau (8 in normal use, a kernel parameter so tests can vary it), so
+// P <= 2^tau and O_t is rescaled in TMEM only on those rare blocks; the result
+// does not depend on tau.  Because m is known before a
 // block's S arrives, P is computed against it as S streams out of TMEM, and the
 // block is redone in the rare case the rule raises m.
 #pragma once
@@ -57,8 +58,7 @@ constexpr int kBN = 128;       // keys per block
 constexpr int kThreads = 320;  // 10 warps
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
-constexpr float kTau = 8.0f;   // lazy-rescale threshold, log2 units
-constexpr float kTwoPowTau = 256.0f;
+constexpr float kTauDefault = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr uint32_t kTmemCols = 512;
 
 // Device status bits (OR-ed into the status word on an abandoned wait).
@@ -104,6 +104,8 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   uint64_t wait_limit_ns;
   int inject;         // 0 in normal use; 1 drops one softmax arrival (timeout test)
+  float tau;          // lazy-rescale threshold (log2 units), 0 <= tau <= 15
+  float two_pow_tau;  // 2^tau
 };
 
 // Shared-memory operand descriptors, 128-byte swizzle.  High half: 8-row groups
@@ -512,16 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // Exponentiate against the running maximum as S arrives from TMEM,
         // one key half at a time.  Every p is at most its half's sum, so a sum
-        // <= 2^kTau proves that no logit of the half exceeds m by more than
-        // kTau and its P stands as computed; only a larger sum (rare once m has
+        // <= 2^tau proves that no logit of the half exceeds m by more than
+        // tau and its P stands as computed; only a larger sum (rare once m has
         // settled: p <= 1 while the block maximum stays below m) needs the
         // exact maximum of that half.
         uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
         float la = exp_keys_lo<BF16>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
-        bool check = la > kTwoPowTau;
+        bool check = la > p.two_pow_tau;
         if (__any_sync(0xffffffffu, check)) {
           const float bmax = row_max<64>(lo) * cl2;
-          const bool raise = check && bmax > m + kTau;
+          const bool raise = check && bmax > m + p.tau;
           if (__any_sync(0xffffffffu, raise)) {
             // O_t holds every earlier block (the commit behind s_full[t] was
             // issued after the previous P_t V): scale it, redo keys 0-63.
@@ -537,11 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += la;
         release(0);
         const float lb = exp_keys_hi<BF16>(hi, tS, c2, negm2, masked_block, lim_blk);
-        check = lb > kTwoPowTau;
+        check = lb > p.two_pow_tau;
         float lhi = lb;
         if (__any_sync(0xffffffffu, check)) {
           const float bmax = row_max<64>(hi) * cl2;
-          const bool raise = check && bmax > m + kTau;
+          const bool raise = check && bmax > m + p.tau;
           if (__any_sync(0xffffffffu, raise)) {
             // Keys 0-63 of this block are already being multiplied into O_t:
             // wait for that half of P V, then scale O_t (it now includes them,
