@@ -81,11 +81,23 @@ def _barrier(dist, device):
 
 
 def _max_over_ranks(dist, x, device):
+    """The slowest rank's time: every rank waits for it (weak scaling)."""
     if dist is None:
         return x
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(w, rank):
+    """Each rank draws its own copy of the workload (its own batch): the
+    (batch, head) slices are independent, so ranks share no data."""
+    return w.seed + 7919 * rank
+
+
+def job_tflops(w, world, ms_per_step):
+    """Whole-job throughput: every rank processed one full workload per step."""
+    return world * w.flops / (ms_per_step / 1e3) / 1e12
 
 
 def _peaks():
@@ -309,7 +321,7 @@ def run_ours(args, w):
     torch.cuda.set_device(device)
     wsa.load_library()
 
-    q, k, v = synthetic.make_inputs_device(w, device, seed=w.seed + 7919 * rank)
+    q, k, v = synthetic.make_inputs_device(w, device, seed=rank_seed(w, rank))
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
@@ -340,7 +352,7 @@ def run_ours(args, w):
         raise SystemExit("device status error in the timed region")
 
     ms_per_step = total_ms / args.steps
-    value = world * w.flops / (ms_per_step / 1e3) / 1e12
+    value = job_tflops(w, world, ms_per_step)
     kernel_ms = statistics.mean(launches)
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
 
@@ -369,7 +381,7 @@ def run_ours(args, w):
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / e2e_steps
-    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+    e2e_value = job_tflops(w, world, e2e_ms)
     # a step's result really is back on the host
     if not (torch.isfinite(hl).all().item() and torch.isfinite(ho[0, 0, :4].float()).all().item()):
         raise SystemExit("end-to-end outputs are not finite")
