@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -23,6 +24,10 @@ namespace {
 __device__ int g_wsa_status = 0;
 
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr int kMaxDevices = 64;
+// Causal unit order: the K and V of one group of heads, read by the units in
+// flight together, are kept to about a quarter of the 129 MB L2.
+constexpr int64_t kGroupKvBytes = int64_t{32} << 20;
 
 thread_local char t_last_cuda_error[256] = "";
 
@@ -74,6 +79,31 @@ bool encode_bhsd(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, bool bf16
   return r == CUDA_SUCCESS;
 }
 
+// Device address of the status word, looked up once per device.
+cudaError_t status_word(int** out) {
+  static std::atomic<int*> cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable) {
+    *out = cache[dev].load(std::memory_order_acquire);
+    if (*out != nullptr) return cudaSuccess;
+  }
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_wsa_status);
+  if (e == cudaSuccess && cacheable) cache[dev].store(*out, std::memory_order_release);
+  return e;
+}
+
+// Heads per group of the causal unit order: as many as keep the group's K and
+// V within kGroupKvBytes, then evened out over the groups.
+int causal_group_heads(int64_t BH, int64_t S, int64_t D) {
+  const int64_t kv_per_head = 2 * S * D * 2;
+  const int64_t cap = std::max<int64_t>(1, kGroupKvBytes / kv_per_head);
+  const int64_t groups = (BH + cap - 1) / cap;
+  return static_cast<int>((BH + groups - 1) / groups);
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -121,7 +151,7 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
 
   int* status = nullptr;
-  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_wsa_status);
+  e = status_word(&status);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
 
   wsa::FwdParams prm;
@@ -130,6 +160,9 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   prm.status = status;
   prm.S = static_cast<int>(S);
   prm.n_qblk = static_cast<int>((S + 255) / 256);
+  prm.BH = static_cast<int>(BH);
+  prm.group_heads = causal ? causal_group_heads(BH, S, D) : 1;
+  prm.dynamic = 1;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = wait_limit_ns;
   prm.inject = inject;
@@ -147,7 +180,6 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
 // Per host thread and device: the two copy streams and the events that chain
 // chunks between them and the caller's stream (created on first use).
 constexpr int kMaxChunks = 64;
-constexpr int kMaxDevices = 64;
 struct HostPipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;

@@ -17,12 +17,30 @@
 // Warp roles (320 threads, one CTA per SM):
 //   warps 0-3  softmax + epilogue, query tile 0 (TMEM lanes 0-127)
 //   warps 4-7  softmax + epilogue, query tile 1
-//   warp  8    TMEM allocator and the single-thread tcgen05.mma issuer
-//   warp  9    TMA producer: Q once, then K_j / V_j through an SMEM ring
+//   warp  8    TMEM allocator and the tcgen05.mma issuer
+//   warp  9    TMA producer and scheduler: per work unit Q, then K_j / V_j
+//              through an SMEM ring
 // The variable-latency TMA loads sit on their own warp and nothing blocking
 // shares a warp with the MMA issuer (the warp-specialization rules of the Twill
 // page, "core method": variable-latency ops on a dedicated warp, no blocking
 // wait beside interruptible ops).
+//
+// Persistent scheduling.  The grid has one block per work unit (head, 256-row
+// query block), but a running block takes further units itself: while it
+// streams one unit, its producer warp asks the hardware (cluster launch
+// control) to cancel a not-yet-started block and adopts that block's unit.
+// So each SM runs one block that moves from unit to unit, the next unit's K/V
+// and Q loads overlap the current unit's last blocks and epilogue, and the
+// order in which units start is the block-index order, which decode_unit()
+// makes longest-first for causal masks.  (Tawa, Section IV-B and Fig. 7(b):
+// resident blocks that iterate over tiles, removing relaunch cost and
+// overlapping loads, tensor-core work and epilogue; the wave count that a
+// one-block-per-tile grid is quantised to is the W of "A Performance Model for
+// Warp Specialization Kernels", core formulas.)  No global counter is involved, so a launch needs no
+// memory beyond its outputs.  The unit travels from the producer to the other
+// roles through a two-slot channel (unit_full / unit_empty); Q tiles are
+// reloaded once the previous unit's last Q K^T is done (q_full / q_empty) and
+// O_t is overwritten only after the previous epilogue read it (o_empty).
 //
 // Synchronisation is the aref channel of the Tawa page (Section III-B/III-E):
 // every ring slot has a full barrier (TMA transaction bytes) and an empty
@@ -48,6 +66,8 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "ptx.cuh"
 
@@ -78,22 +98,30 @@ struct Cfg {
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingOff = kQBytes;
   static constexpr int kCtlOff = kRingOff + kStages * kSlotBytes;
-  static constexpr int kSmemBytes = 1024 + kCtlOff + 256;  // + alignment slack + control
+  static constexpr int kSmemBytes = 1024 + kCtlOff + 512;  // + alignment slack + control
   static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
 };
 
 struct Ctl {
+  uint4 clc_answer;        // cluster-launch-control answer (16-byte aligned)
+  uint64_t clc_bar;        // its 16 transaction bytes
+  uint64_t unit_full[2];   // work-unit channel, loader -> MMA and softmax warps
+  uint64_t unit_empty[2];
+  int unit_id[2];          // unit index, or -1: no more work
   uint64_t q_full;
+  uint64_t q_empty;        // Q tiles consumed by the unit's last Q K^T
   uint64_t s_full[2];
   uint64_t p_half[2][2];   // [tile][key half]: P of keys 64h..64h+63 is in TMEM
   uint64_t pva_done[2];    // [tile]: the P V of keys 0-63 of the current block is done
   uint64_t o_full[2];
+  uint64_t o_empty[2];     // [tile]: the epilogue has read O_t out of TMEM
   uint64_t mma_drain;
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Ctl) <= 512, "control block size");
 
 struct FwdParams {
   void* o;            // (B,H,S,D) 16-bit
@@ -101,12 +129,47 @@ struct FwdParams {
   int* status;        // device status word
   int S;
   int n_qblk;         // ceil(S / 256)
+  int BH;             // B * H
+  int group_heads;    // causal unit order: heads per L2 group (>= 1)
+  int dynamic;        // 1: blocks take further units by cluster launch control
   float scale_log2;   // scale * log2(e)
   uint64_t wait_limit_ns;
   int inject;         // 0 in normal use; 1 drops one softmax arrival (timeout test)
   float tau;          // lazy-rescale threshold (log2 units), 0 <= tau <= 15
   float two_pow_tau;  // 2^tau
 };
+
+// A work unit: one (batch*head) index and one 256-row query block.
+struct Unit {
+  int bh;
+  int qb;
+};
+
+// Unit index -> (head, query block); the grid has one block per unit and the
+// hardware starts (or hands over) blocks in index order, so this fixes the
+// order in which units begin.  Full attention: head-major, every unit costs
+// the same.  Causal: unit qb costs 2qb+1 or 2qb+2 key blocks, so heads are
+// taken in groups whose K and V fit in L2 together and, inside a group, the
+// longest query blocks of all its heads go first (longest-processing-time-first
+// list scheduling) -- the schedule that shortens the tail, without making K/V
+// of a head leave L2 between its units.
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int x, const FwdParams& p) {
+  Unit u;
+  if (!CAUSAL) {
+    u.bh = x / p.n_qblk;
+    u.qb = x - u.bh * p.n_qblk;
+    return u;
+  }
+  const int per_group = p.group_heads * p.n_qblk;
+  const int g = x / per_group;
+  const int r = x - g * per_group;
+  const int gh = min(p.group_heads, p.BH - g * p.group_heads);
+  const int level = r / gh;
+  u.bh = g * p.group_heads + (r - level * gh);
+  u.qb = p.n_qblk - 1 - level;
+  return u;
+}
 
 // Shared-memory operand descriptors, 128-byte swizzle.  High half: 8-row groups
 // 1024 bytes apart.  Low half: start address plus the leading byte offset,
@@ -304,25 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: (head bh, 256-row query block qb)
   const int S = p.S;
-  const int bh = blockIdx.x / p.n_qblk;
-  int qb = blockIdx.x - bh * p.n_qblk;
-  if (CAUSAL) qb = p.n_qblk - 1 - qb;  // longest rows first within a head
-  const int q0 = qb * 2 * kBM;
   const int nkv_all = (S + kBN - 1) / kBN;
-  const int nkv0 = CAUSAL ? min(nkv_all, 2 * qb + 1) : nkv_all;
-  const int nkv1 = CAUSAL ? min(nkv_all, 2 * qb + 2) : nkv_all;
+  // key blocks of query tile 0 / tile 1 of query block qb
+  auto nkv_tile0 = [&](int qb) { return CAUSAL ? min(nkv_all, 2 * qb + 1) : nkv_all; };
+  auto nkv_tile1 = [&](int qb) { return CAUSAL ? min(nkv_all, 2 * qb + 2) : nkv_all; };
 
   if (threadIdx.x == 0) {
+    mbar_init(&ctl.clc_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.unit_full[i], 1);
+      mbar_init(&ctl.unit_empty[i], 9);  // the MMA warp and the 8 softmax warps
+    }
     mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.q_empty, 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl.s_full[t], 1);
       mbar_init(&ctl.p_half[t][0], 4);  // one elected arrival per softmax warp
       mbar_init(&ctl.p_half[t][1], 4);
       mbar_init(&ctl.pva_done[t], 1);
       mbar_init(&ctl.o_full[t], 1);
+      mbar_init(&ctl.o_empty[t], 4);
     }
     mbar_init(&ctl.mma_drain, 1);
     for (int s = 0; s < C::kStages; ++s) {
@@ -345,6 +410,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = sbase;
   const uint32_t sRing = sbase + C::kRingOff;
 
+  // The k-th unit of this block (k = 0, 1, ...) travels from the loader to the
+  // other roles through slot k & 1 of the unit channel; -1 ends the loop.
+  auto next_unit = [&](uint32_t k, int code, int* out) {
+    bool ok = mbar_wait(&ctl.unit_full[k & 1], (k >> 1) & 1, abort_flag, p.status, code,
+                        p.wait_limit_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    *out = *reinterpret_cast<volatile int*>(&ctl.unit_id[k & 1]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl.unit_empty[k & 1]);
+    return true;
+  };
+
   if (warp == kWarpLoad) {
     // ================================================================ TMA producer
     // The whole warp runs the loop; one elected lane issues each copy.
@@ -353,31 +431,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
     const uint64_t pol_q = policy_evict_first();
     const uint64_t pol_kv = policy_evict_last();
-    mbar_arrive_expect_tx_warp(&ctl.q_full, 2 * C::kTileBytes);
-    for (int t = 0; t < 2; ++t)
-      for (int cb = 0; cb < D / 64; ++cb)
-        tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full, cb * 64,
-                         q0 + t * kBM, bh, pol_q);
-    uint32_t it = 0;  // ring item: K_j is item 2j, V_j is item 2j+1
+    const uint32_t clc_answer = smem_u32(&ctl.clc_answer);
+    uint32_t it = 0;         // ring item: K_j of a unit, then V_j, block after block
+    uint32_t nq = 0;         // Q loads issued
+    uint32_t asked = 0;      // cancellation requests issued
+    uint32_t answered = 0;   // ... and their answers read
     bool ok = true;
-    for (int j = 0; ok && j < nkv1; ++j) {
-      for (int kv = 0; kv < 2; ++kv) {
-        const uint32_t slot = it % C::kStages;
-        const uint32_t use = it / C::kStages;
-        ok = mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
-                       kStatusTimeoutLoad, p.wait_limit_ns);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
-        const CUtensorMap* m = kv ? &tm_v : &tm_k;
-        for (int cb = 0; cb < D / 64; ++cb)
-          tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m, &ctl.kv_full[slot],
-                           cb * 64, j * kBN, bh, pol_kv);
-        ++it;
+    int x = blockIdx.x;
+    for (uint32_t k = 0; ok; ++k) {
+      ok = mbar_wait(&ctl.unit_empty[k & 1], ((k >> 1) & 1) ^ 1, abort_flag, p.status,
+                     kStatusTimeoutLoad, p.wait_limit_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        ctl.unit_id[k & 1] = x;
+        mbar_arrive(&ctl.unit_full[k & 1]);
       }
+      __syncwarp();
+      if (x < 0) break;
+      const Unit u = decode_unit<CAUSAL>(x, p);
+      const int q0 = u.qb * 2 * kBM;
+      const int nkv1 = nkv_tile1(u.qb);
+      if (p.dynamic) {
+        // ask for the next unit now; the answer is read half-way through this one
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx_warp(&ctl.clc_bar, 16);
+        clc_try_cancel_warp(clc_answer, &ctl.clc_bar);
+        ++asked;
+      }
+      int x_next = -1;
+      for (int j = 0; ok && j < nkv1; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t slot = it % C::kStages;
+          const uint32_t use = it / C::kStages;
+          ok = mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
+                         kStatusTimeoutLoad, p.wait_limit_ns);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
+          const CUtensorMap* m = kv ? &tm_v : &tm_k;
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m,
+                             &ctl.kv_full[slot], cb * 64, j * kBN, u.bh, pol_kv);
+          ++it;
+          if (j == 0 && kv == 1) {
+            // Q after K_0 and V_0: the previous unit's last Q K^T frees the
+            // Q tiles while this unit's first K/V are already in flight.
+            ok = mbar_wait(&ctl.q_empty, (nq & 1) ^ 1, abort_flag, p.status, kStatusTimeoutLoad,
+                           p.wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            mbar_arrive_expect_tx_warp(&ctl.q_full, 2 * C::kTileBytes);
+            for (int t = 0; t < 2; ++t)
+              for (int cb = 0; cb < D / 64; ++cb)
+                tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full,
+                                 cb * 64, q0 + t * kBM, u.bh, pol_q);
+            ++nq;
+          }
+          if (p.dynamic && j == nkv1 / 2 && kv == 1) {
+            ok = mbar_wait(&ctl.clc_bar, answered & 1, abort_flag, p.status, kStatusTimeoutLoad,
+                           p.wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            x_next = clc_cancelled_x(clc_answer);
+            ++answered;
+            if (x_next >= 0) {
+              // the next unit's Q into L2 while this unit still streams
+              const Unit un = decode_unit<CAUSAL>(x_next, p);
+              for (int t = 0; t < 2; ++t)
+                for (int cb = 0; cb < D / 64; ++cb)
+                  tma_prefetch_3d_warp(&tm_q, cb * 64, un.qb * 2 * kBM + t * kBM, un.bh);
+            }
+          }
+        }
+      }
+      x = x_next;
     }
-    // Drain: every issued copy lands before the block may exit.
-    mbar_wait(&ctl.q_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    // Drain: every issued copy and request lands before the block may exit.
+    if (asked > answered)
+      mbar_wait(&ctl.clc_bar, answered & 1, nullptr, p.status, kStatusTimeoutDrain,
+                p.wait_limit_ns);
+    if (nq > 0)
+      mbar_wait(&ctl.q_full, (nq - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
+                p.wait_limit_ns);
     const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
     for (uint32_t i = first; i < it; ++i)
       mbar_wait(&ctl.kv_full[i % C::kStages], (i / C::kStages) & 1, nullptr, p.status,
@@ -404,51 +540,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O_t += P_t V in two key halves, each as soon as its P is in TMEM; the
     // first half's completion is committed for a softmax that has to rescale
-    // O_t while computing the second half.
-    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, int j) {
-      if (!wait(&ctl.p_half[t][0], j & 1)) return false;
+    // O_t while computing the second half.  g = the tile's block count over
+    // all units of this block (P phases); the first P V of a unit overwrites
+    // O_t, so it waits until the previous unit's epilogue has read O_t.
+    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t g, int j,
+                         uint32_t k) {
+      if (j == 0 && !wait(&ctl.o_empty[t], (k & 1) ^ 1)) return false;
+      if (!wait(&ctl.p_half[t][0], g & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, BF16>(tO, tS, vlo, 0, j > 0);
       mma_commit_warp(&ctl.pva_done[t]);
-      if (!wait(&ctl.p_half[t][1], j & 1)) return false;
+      if (!wait(&ctl.p_half[t][1], g & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, BF16>(tO, tS, vlo, 1, true);
       return true;
     };
-    bool ok = wait(&ctl.q_full, 0);
-    ok = ok && wait_full(0);
-    if (ok) {
+    bool ok = true;
+    uint32_t it = 0;          // ring item of the unit's K_0
+    uint32_t g0 = 0, g1 = 0;  // key blocks done by tile 0 / tile 1
+    for (uint32_t k = 0; ok; ++k) {
+      int x;
+      ok = next_unit(k, kStatusTimeoutMma, &x);
+      if (!ok || x < 0) break;
+      const Unit u = decode_unit<CAUSAL>(x, p);
+      const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
+      ok = wait_full(it) && wait(&ctl.q_full, k & 1);
+      if (!ok) break;
       tc_fence_after();
-      issue_qk<D, BF16>(tS0, q0_lo, k_lo(0));
+      issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
       mma_commit_warp(&ctl.s_full[0]);
-      issue_qk<D, BF16>(tS1, q1_lo, k_lo(0));
+      issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
       mma_commit_warp(&ctl.s_full[1]);
-      mma_commit_warp(&ctl.kv_empty[0]);
-    }
-    for (int j = 0; ok && j < nkv1; ++j) {
-      const uint32_t iv = 2 * j + 1, ik = 2 * j + 2;
-      const bool more = j + 1 < nkv1;
-      if (!wait_full(iv)) break;
-      if (j < nkv0) {
-        if (!pv_halves(0, tO0, tS0, v_lo(iv), j)) break;
-        if (j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
-      }
-      if (more) {
-        if (!wait_full(ik)) break;
-        tc_fence_after();
-        if (j + 1 < nkv0) {
-          issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
-          mma_commit_warp(&ctl.s_full[0]);
+      mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
+      if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
+      for (int j = 0; ok && j < nkv1; ++j) {
+        const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
+        const bool more = j + 1 < nkv1;
+        ok = wait_full(iv);
+        if (ok && j < nkv0) {
+          ok = pv_halves(0, tO0, tS0, v_lo(iv), g0 + j, j, k);
+          if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
+        }
+        if (ok && more) {
+          ok = wait_full(ik);
+          tc_fence_after();
+          if (ok && j + 1 < nkv0) {
+            issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
+            mma_commit_warp(&ctl.s_full[0]);
+          }
+        }
+        ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j, k);
+        if (!ok) break;
+        mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
+        if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
+        if (more) {
+          issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+          mma_commit_warp(&ctl.s_full[1]);
+          mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
+          if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
         }
       }
-      if (!pv_halves(1, tO1, tS1, v_lo(iv), j)) break;
-      mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
-      if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
-      if (more) {
-        issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
-        mma_commit_warp(&ctl.s_full[1]);
-        mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
-      }
+      it += 2 * nkv1;
+      g0 += nkv0;
+      g1 += nkv1;
     }
     // Drain: all issued MMAs complete before TMEM can be released.
     mma_commit_warp(&ctl.mma_drain);
@@ -458,129 +612,137 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax tile t
     const int t = warp >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
-    const int row = q0 + t * kBM + quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t tS = lane_base + t * kBM;
     const uint32_t tO = lane_base + C::kOCol + t * D;
-    const int nkv = t ? nkv1 : nkv0;
     const float cl2 = p.scale_log2;
-    // keys visible to this row: [0, lim)
-    const int lim = CAUSAL ? min(row + 1, S) : S;
-
-    float m = -INFINITY;  // running maximum, log2 units of the scaled logits
-    float l = 0.f;        // running sum of exp2(s*c - m)
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      ok = mbar_wait(&ctl.s_full[t], j & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
-                     p.wait_limit_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
+    uint32_t g = 0;  // key blocks done by this tile over all units of the block
+    for (uint32_t k = 0; ok; ++k) {
+      int x;
+      ok = next_unit(k, kStatusTimeoutSoftmax, &x);
+      if (!ok || x < 0) break;
+      const Unit u = decode_unit<CAUSAL>(x, p);
+      const int row = u.qb * 2 * kBM + t * kBM + quad * 32 + lane;
+      const int nkv = t ? nkv_tile1(u.qb) : nkv_tile0(u.qb);
+      // keys visible to this row: [0, lim)
+      const int lim = CAUSAL ? min(row + 1, S) : S;
 
-      const bool masked_block = (j == nkv - 1) && (CAUSAL || (S % kBN) != 0);
-      const int lim_blk = lim - j * kBN;
-      uint32_t lo[64], hi[64];
-      // Hands one key half of P to the MMA issuer once its stores have landed.
-      auto release = [&](int half) {
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && !(p.inject == 1 && t == 0 && j == 0 && half == 0))
-          mbar_arrive(&ctl.p_half[t][half]);
-      };
-      // O_t *= alpha for threads with alpha != 1 (all lanes take part).
-      auto rescale_o = [&](float alpha) {
+      float m = -INFINITY;  // running maximum, log2 units of the scaled logits
+      float l = 0.f;        // running sum of exp2(s*c - m)
+      for (int j = 0; j < nkv; ++j) {
+        const uint32_t ph = (g + j) & 1;
+        ok = mbar_wait(&ctl.s_full[t], ph, abort_flag, p.status, kStatusTimeoutSoftmax,
+                       p.wait_limit_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+
+        const bool masked_block = (j == nkv - 1) && (CAUSAL || (S % kBN) != 0);
+        const int lim_blk = lim - j * kBN;
+        uint32_t lo[64], hi[64];
+        // Hands one key half of P to the MMA issuer once its stores have landed.
+        auto release = [&](int half) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && !(p.inject == 1 && t == 0 && k == 0 && j == 0 && half == 0))
+            mbar_arrive(&ctl.p_half[t][half]);
+        };
+        // O_t *= alpha for threads with alpha != 1 (all lanes take part).
+        auto rescale_o = [&](float alpha) {
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t orr[32];
-          tmem_ld_x32(tO + ch * 32, orr);
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t orr[32];
+            tmem_ld_x32(tO + ch * 32, orr);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st_x32(tO + ch * 32, orr);
-        }
-      };
-      if (j == 0) {
-        // First block: no running maximum yet, so take the block maximum first.
-        load_s(tS, lo, hi);
-        if (masked_block) {
-          mask_keys<0, 64>(lo, lim_blk);
-          mask_keys<64, 64>(hi, lim_blk);
-        }
-        m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
-        l = exp_keys_regs<BF16>(lo, cl2, m, tS);
-        release(0);
-        l += exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
-        release(1);
-      } else {
-        // Exponentiate against the running maximum as S arrives from TMEM,
-        // one key half at a time.  Every p is at most its half's sum, so a sum
-        // <= 2^tau proves that no logit of the half exceeds m by more than
-        // tau and its P stands as computed; only a larger sum (rare once m has
-        // settled: p <= 1 while the block maximum stays below m) needs the
-        // exact maximum of that half.
-        uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
-        float la = exp_keys_lo<BF16>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
-        bool check = la > p.two_pow_tau;
-        if (__any_sync(0xffffffffu, check)) {
-          const float bmax = row_max<64>(lo) * cl2;
-          const bool raise = check && bmax > m + p.tau;
-          if (__any_sync(0xffffffffu, raise)) {
-            // O_t holds every earlier block (the commit behind s_full[t] was
-            // issued after the previous P_t V): scale it, redo keys 0-63.
-            const float alpha = raise ? ex2(m - bmax) : 1.f;
-            if (raise) m = bmax;
-            l *= alpha;
-            tmem_st_wait();
-            la = exp_keys_regs<BF16>(lo, cl2, m, tS);
-            rescale_o(alpha);
-            negm2 = f2_pack(-m, -m);
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st_x32(tO + ch * 32, orr);
           }
-        }
-        l += la;
-        release(0);
-        const float lb = exp_keys_hi<BF16>(hi, tS, c2, negm2, masked_block, lim_blk);
-        check = lb > p.two_pow_tau;
-        float lhi = lb;
-        if (__any_sync(0xffffffffu, check)) {
-          const float bmax = row_max<64>(hi) * cl2;
-          const bool raise = check && bmax > m + p.tau;
-          if (__any_sync(0xffffffffu, raise)) {
-            // Keys 0-63 of this block are already being multiplied into O_t:
-            // wait for that half of P V, then scale O_t (it now includes them,
-            // as does l) and redo keys 64-127 against the raised maximum.
-            bool good = mbar_wait(&ctl.pva_done[t], j & 1, abort_flag, p.status,
-                                  kStatusTimeoutSoftmax, p.wait_limit_ns);
-            good = __all_sync(0xffffffffu, good);
-            if (!good) {
-              ok = false;
-              break;
+        };
+        if (j == 0) {
+          // First block: no running maximum yet, so take the block maximum first.
+          load_s(tS, lo, hi);
+          if (masked_block) {
+            mask_keys<0, 64>(lo, lim_blk);
+            mask_keys<64, 64>(hi, lim_blk);
+          }
+          m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
+          l = exp_keys_regs<BF16>(lo, cl2, m, tS);
+          release(0);
+          l += exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+          release(1);
+        } else {
+          // Exponentiate against the running maximum as S arrives from TMEM,
+          // one key half at a time.  Every p is at most its half's sum, so a sum
+          // <= 2^tau proves that no logit of the half exceeds m by more than
+          // tau and its P stands as computed; only a larger sum (rare once m has
+          // settled: p <= 1 while the block maximum stays below m) needs the
+          // exact maximum of that half.
+          uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
+          float la = exp_keys_lo<BF16>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
+          bool check = la > p.two_pow_tau;
+          if (__any_sync(0xffffffffu, check)) {
+            const float bmax = row_max<64>(lo) * cl2;
+            const bool raise = check && bmax > m + p.tau;
+            if (__any_sync(0xffffffffu, raise)) {
+              // O_t holds every earlier block (the commit behind s_full[t] was
+              // issued after the previous P_t V): scale it, redo keys 0-63.
+              const float alpha = raise ? ex2(m - bmax) : 1.f;
+              if (raise) m = bmax;
+              l *= alpha;
+              tmem_st_wait();
+              la = exp_keys_regs<BF16>(lo, cl2, m, tS);
+              rescale_o(alpha);
+              negm2 = f2_pack(-m, -m);
             }
-            tc_fence_after();
-            const float alpha = raise ? ex2(m - bmax) : 1.f;
-            if (raise) m = bmax;
-            l *= alpha;
-            tmem_st_wait();
-            lhi = exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
-            rescale_o(alpha);
           }
+          l += la;
+          release(0);
+          const float lb = exp_keys_hi<BF16>(hi, tS, c2, negm2, masked_block, lim_blk);
+          check = lb > p.two_pow_tau;
+          float lhi = lb;
+          if (__any_sync(0xffffffffu, check)) {
+            const float bmax = row_max<64>(hi) * cl2;
+            const bool raise = check && bmax > m + p.tau;
+            if (__any_sync(0xffffffffu, raise)) {
+              // Keys 0-63 of this block are already being multiplied into O_t:
+              // wait for that half of P V, then scale O_t (it now includes them,
+              // as does l) and redo keys 64-127 against the raised maximum.
+              bool good = mbar_wait(&ctl.pva_done[t], ph, abort_flag, p.status,
+                                    kStatusTimeoutSoftmax, p.wait_limit_ns);
+              good = __all_sync(0xffffffffu, good);
+              if (!good) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const float alpha = raise ? ex2(m - bmax) : 1.f;
+              if (raise) m = bmax;
+              l *= alpha;
+              tmem_st_wait();
+              lhi = exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+              rescale_o(alpha);
+            }
+          }
+          l += lhi;
+          release(1);
         }
-        l += lhi;
-        release(1);
       }
-    }
+      g += nkv;
 
-    // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
-    if (ok) {
-      ok = mbar_wait(&ctl.o_full[t], 0, abort_flag, p.status, kStatusTimeoutSoftmax,
-                     p.wait_limit_ns);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
+      // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
+      if (ok) {
+        ok = mbar_wait(&ctl.o_full[t], k & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
+                       p.wait_limit_ns);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (!ok) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool store = row < S;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      ((static_cast<size_t>(bh) * S + (store ? row : 0)) * D) * 2;
+                      ((static_cast<size_t>(u.bh) * S + (store ? row : 0)) * D) * 2;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t orr[32];
@@ -597,8 +759,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
         }
       }
+      // O_t has left TMEM: the next unit's first P V may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.o_empty[t]);
       if (store)
-        p.lse[static_cast<size_t>(bh) * S + row] = (m + lg2(l)) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(u.bh) * S + row] = (m + lg2(l)) * 0.69314718055994530942f;
     }
   }
 
@@ -611,13 +777,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Dynamic shared memory above 48 KB is opted into once per device.  Internal
+// linkage keeps the flags private to each loaded copy of the library (a
+// function-local static of an inline template would otherwise become one
+// process-wide symbol shared by every copy).
 template <int D, bool BF16, bool CAUSAL>
-cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& prm, unsigned grid, cudaStream_t stream) {
   auto kern = fmha_fwd_kernel<D, BF16, CAUSAL>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> opted_in[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
+  }
   kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }

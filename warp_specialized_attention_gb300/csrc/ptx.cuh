@@ -267,6 +267,55 @@ __device__ __forceinline__ void tma_load_3d_warp(uint32_t dst_smem, const CUtens
       : "memory");
 }
 
+// Pull one 3-D tile into L2 ahead of its shared-memory load (no completion).
+__device__ __forceinline__ void tma_prefetch_3d_warp(const CUtensorMap* map, int c0, int c1,
+                                                     int c2) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// A running block asks the hardware to cancel the launch of a block of the same
+// grid that has not started yet and to hand over its index: dynamic persistent
+// scheduling with no counter in global memory.  The 16-byte answer lands in
+// shared memory and completes 16 transaction bytes on `bar`.
+
+// Orders this thread's generic-proxy reads of the answer buffer before the
+// async-proxy write of the next answer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void clc_try_cancel_warp(uint32_t resp_smem, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];\n\t}" ::"r"(resp_smem),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// blockIdx.x of the cancelled block, or -1 when the request found none left.
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp_smem) {
+  int x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t.reg .b32 cx;\n\t"
+      "ld.shared.b128 r, [%1];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 cx, r;\n\t"
+      "selp.b32 %0, cx, -1, p;\n\t}"
+      : "=r"(x)
+      : "r"(resp_smem)
+      : "memory");
+  return x;
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
