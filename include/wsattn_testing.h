@@ -28,7 +28,7 @@ extern "C" {
  *                    Outputs are undefined.
  *   wait_limit_s  per-wait time limit in seconds, in (0, 60]; fmha_fwd uses 1.
  *   tau           lazy-rescale threshold of the online softmax in log2 units,
- *                 in [0, 15]; fmha_fwd uses 8.  The running maximum is raised
+ *                 in [0, 15]; fmha_fwd uses 15.  The running maximum is raised
  *                 (and O rescaled) only when a block's maximum exceeds it by more
  *                 than tau, so P <= 2^tau (15 keeps P inside the f16 range).  The
  *                 result does not depend on tau; 0 gives the classic online

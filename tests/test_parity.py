@@ -72,17 +72,28 @@ def test_small_full_compare(case):
     assert eo <= TOL_O and el <= TOL_LSE, "max err O %g LSE %g" % (eo, el)
 
 
+@pytest.mark.parametrize("tau", [None, 8.0], ids=["tau-default", "tau-8"])
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_rising_maximum_forces_rescale(dt, causal):
-    """K is multiplied by 2 per key block, so the running maximum of many rows
-    jumps by more than the lazy-rescale threshold on block after block: this
-    drives the redo-and-rescale path of the online softmax."""
+def test_rising_maximum_forces_rescale(dt, causal, tau):
+    """K is multiplied by 2 per key block, so the block maxima of the scaled
+    logits (log2 units, median over rows) grow 0.9, 1.8, 3.6, ..., 58 over the
+    seven blocks: at the default threshold (15) the running maximum of every
+    row is raised twice (blocks 5 and 6), at tau = 8 about three times, each
+    time by a large factor.  This drives the redo-and-rescale path of the
+    online softmax."""
     w = synthetic.Workload("ramp", 1, 2, 896, 128, dt, causal, 1.0, 808)
     q, k, v = synthetic.make_inputs(w)
     mult = (2.0 ** (torch.arange(w.S) // 128)).to(k.dtype)   # 1, 2, ..., 64 per block
     k = (k * mult[None, None, :, None] / 4).to(k.dtype)
-    o, lse = _gpu(q, k, v, causal, w.scale)
+    if tau is None:
+        o, lse = _gpu(q, k, v, causal, w.scale)
+    else:
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o = torch.full_like(qd, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), device="cuda", dtype=torch.float32)
+        assert wsa.fmha_fwd_testing(qd, kd, vd, o, lse, causal, w.scale, 0, 1.0, tau) == wsa.FMHA_OK
+        assert wsa.get_device_status() == wsa.FMHA_OK
     o_ref, lse_ref = oracle.attention(q.double().numpy(), k.double().numpy(),
                                       v.double().numpy(), causal, w.scale)
     eo, el = _errors(o.cpu(), lse.cpu(), o_ref, lse_ref)
@@ -92,8 +103,8 @@ def test_rising_maximum_forces_rescale(dt, causal):
     # |dO| <= u*max|V| + u*max|O| (+ fp32 and exp2 error, well under 1e-3).
     u = 2.0 ** -8 if dt == "bf16" else 2.0 ** -11
     tol_o = u * float(v.abs().max()) + u * float(np.abs(o_ref).max()) + 1e-3
-    print("PARITY rising-max %s %s max_err_O %.3e (bound %.3e) max_err_LSE %.3e"
-          % (dt, "causal" if causal else "full", eo, tol_o, el))
+    print("PARITY rising-max %s %s tau=%s max_err_O %.3e (bound %.3e) max_err_LSE %.3e"
+          % (dt, "causal" if causal else "full", tau, eo, tol_o, el))
     assert eo <= tol_o and el <= TOL_LSE, "max err O %g LSE %g" % (eo, el)
 
 
@@ -172,8 +183,8 @@ def test_scale_is_applied():
 def test_result_independent_of_lazy_rescale_threshold(case):
     """tau = 0 is the classic online softmax (rescale whenever the maximum
     grows, which also drives the exact-maximum check on nearly every block);
-    tau = 8 is the default lazy rule; tau = 15 the largest allowed.  All must
-    match the oracle, and each other to within rounding."""
+    tau = 8 a moderate lazy rule; tau = 15 the largest allowed and the default.
+    All must match the oracle, and each other to within rounding."""
     B, H, S, D, dt, causal, k_mult = case
     w = synthetic.Workload("tau", B, H, S, D, dt, causal, k_mult, 9000 + S)
     q, k, v = synthetic.make_inputs(w)

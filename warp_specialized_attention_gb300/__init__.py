@@ -182,7 +182,7 @@ def fmha_fwd_host(q, k, v, o, lse, dq, dk, dv, d_o, dlse, causal: bool = False,
 
 
 def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: int,
-                     wait_limit_s: float, tau: float = 8.0, stream=None) -> int:
+                     wait_limit_s: float, tau: float = 15.0, stream=None) -> int:
     """Test hook of include/wsattn_testing.h; returns the raw status code."""
     lib = load_library()
     _check(q, k, v, o, lse)

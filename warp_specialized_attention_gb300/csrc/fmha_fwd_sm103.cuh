@@ -58,11 +58,14 @@
 //
 // Online softmax with a lazy maximum: the running maximum m (in log2 units of
 // the scaled logits) is only raised when a block's maximum exceeds it by more
-// than tau (8 in normal use, a kernel parameter so tests can vary it), so
-// P <= 2^tau and O_t is rescaled in TMEM only on those rare blocks; the result
-// does not depend on tau.  Because m is known before a
+// than tau, so P <= 2^tau and O_t is rescaled in TMEM only on those rare
+// blocks; the result does not depend on tau.  Because m is known before a
 // block's S arrives, P is computed against it as S streams out of TMEM, and the
-// block is redone in the rare case the rule raises m.
+// block is redone in the rare case the rule raises m.  tau = 15 is the largest
+// value that keeps every P finite in f16 (2^15 < 65504); the larger tau, the
+// rarer a redo: with logits four times as spread as N(0,1) inputs give, tau = 8
+// redoes often enough to cost a quarter of the throughput at D = 64.  (tau is a
+// kernel parameter so tests can vary it.)
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -78,7 +81,7 @@ constexpr int kBN = 128;       // keys per block
 constexpr int kThreads = 320;  // 10 warps
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
-constexpr float kTauDefault = 8.0f;  // lazy-rescale threshold, log2 units
+constexpr float kTauDefault = 15.0f;  // lazy-rescale threshold, log2 units
 constexpr uint32_t kTmemCols = 512;
 
 // Device status bits (OR-ed into the status word on an abandoned wait).
@@ -541,11 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O_t += P_t V in two key halves, each as soon as its P is in TMEM; the
     // first half's completion is committed for a softmax that has to rescale
     // O_t while computing the second half.  g = the tile's block count over
-    // all units of this block (P phases); the first P V of a unit overwrites
-    // O_t, so it waits until the previous unit's epilogue has read O_t.
-    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t g, int j,
-                         uint32_t k) {
-      if (j == 0 && !wait(&ctl.o_empty[t], (k & 1) ^ 1)) return false;
+    // all units of this block (P phases).
+    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t g, int j) {
       if (!wait(&ctl.p_half[t][0], g & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, BF16>(tO, tS, vlo, 0, j > 0);
@@ -573,12 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_warp(&ctl.s_full[1]);
       mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
       if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
+      // The unit's first P V overwrites O_0 and O_1: the previous unit's
+      // epilogue must have read them (waited here, outside the block loop).
+      ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
       for (int j = 0; ok && j < nkv1; ++j) {
         const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
         const bool more = j + 1 < nkv1;
         ok = wait_full(iv);
         if (ok && j < nkv0) {
-          ok = pv_halves(0, tO0, tS0, v_lo(iv), g0 + j, j, k);
+          ok = pv_halves(0, tO0, tS0, v_lo(iv), g0 + j, j);
           if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
         }
         if (ok && more) {
@@ -589,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_warp(&ctl.s_full[0]);
           }
         }
-        ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j, k);
+        ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j);
         if (!ok) break;
         mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
         if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
