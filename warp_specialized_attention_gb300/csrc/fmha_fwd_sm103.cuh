@@ -103,6 +103,11 @@ struct Cfg {
   static constexpr int kCtlOff = kRingOff + kStages * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kCtlOff + 512;  // + alignment slack + control
   static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
+  // D = 64 leaves 128 TMEM columns free: P_t gets its own 64 columns there
+  // (split P), so S_t can be overwritten as soon as the softmax has read it.
+  static constexpr bool kSplitP = D == 64;
+  static constexpr uint32_t kPCol = 256 + 2 * D;           // split P_t at kPCol + 64t
+  static_assert(!kSplitP || kPCol + 128 <= 512, "TMEM columns");
 };
 
 struct Ctl {
@@ -116,6 +121,8 @@ struct Ctl {
   uint64_t s_full[2];
   uint64_t p_half[2][2];   // [tile][key half]: P of keys 64h..64h+63 is in TMEM
   uint64_t pva_done[2];    // [tile]: the P V of keys 0-63 of the current block is done
+  uint64_t pvb_done[2];    // [tile]: ... of keys 64-127 (split P only)
+  uint64_t s_free[2];      // [tile]: the softmax has read S_t (split P only)
   uint64_t o_full[2];
   uint64_t o_empty[2];     // [tile]: the epilogue has read O_t out of TMEM
   uint64_t mma_drain;
@@ -389,6 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.p_half[t][0], 4);  // one elected arrival per softmax warp
       mbar_init(&ctl.p_half[t][1], 4);
       mbar_init(&ctl.pva_done[t], 1);
+      mbar_init(&ctl.pvb_done[t], 1);
+      mbar_init(&ctl.s_free[t], 4);
       mbar_init(&ctl.o_full[t], 1);
       mbar_init(&ctl.o_empty[t], 4);
     }
@@ -545,14 +554,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first half's completion is committed for a softmax that has to rescale
     // O_t while computing the second half.  g = the tile's block count over
     // all units of this block (P phases).
-    auto pv_halves = [&](int t, uint32_t tO, uint32_t tS, uint32_t vlo, uint32_t g, int j) {
+    auto pv_halves = [&](int t, uint32_t tO, uint32_t tP, uint32_t vlo, uint32_t g, int j) {
       if (!wait(&ctl.p_half[t][0], g & 1)) return false;
       tc_fence_after();
-      issue_pv_half<D, BF16>(tO, tS, vlo, 0, j > 0);
+      issue_pv_half<D, BF16>(tO, tP, vlo, 0, j > 0);
       mma_commit_warp(&ctl.pva_done[t]);
       if (!wait(&ctl.p_half[t][1], g & 1)) return false;
       tc_fence_after();
-      issue_pv_half<D, BF16>(tO, tS, vlo, 1, true);
+      issue_pv_half<D, BF16>(tO, tP, vlo, 1, true);
+      if constexpr (C::kSplitP) mma_commit_warp(&ctl.pvb_done[t]);
       return true;
     };
     bool ok = true;
@@ -566,41 +576,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
       ok = wait_full(it) && wait(&ctl.q_full, k & 1);
       if (!ok) break;
-      tc_fence_after();
-      issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
-      mma_commit_warp(&ctl.s_full[0]);
-      issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
-      mma_commit_warp(&ctl.s_full[1]);
-      mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
-      if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
-      // The unit's first P V overwrites O_0 and O_1: the previous unit's
-      // epilogue must have read them (waited here, outside the block loop).
-      ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
-      for (int j = 0; ok && j < nkv1; ++j) {
-        const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
-        const bool more = j + 1 < nkv1;
-        ok = wait_full(iv);
-        if (ok && j < nkv0) {
-          ok = pv_halves(0, tO0, tS0, v_lo(iv), g0 + j, j);
-          if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
-        }
-        if (ok && more) {
-          ok = wait_full(ik);
-          tc_fence_after();
-          if (ok && j + 1 < nkv0) {
+      if constexpr (C::kSplitP) {
+        // Split P: Q K^T of tile t waits only until the softmax has read the
+        // previous S_t, so a tile's next S is computed while its softmax still
+        // works on the current block.  Per block j the issue order is
+        // S_0(j+1), P_0 V_j, S_1(j+1), P_1 V_j: each tile's P V is issued as
+        // soon as its P is in TMEM, never behind a wait on the other tile.
+        const uint32_t tP0 = tmem + C::kPCol, tP1 = tmem + C::kPCol + 64;
+        ok = (g0 == 0 || wait(&ctl.s_free[0], (g0 - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
+        mma_commit_warp(&ctl.s_full[0]);
+        ok = (g1 == 0 || wait(&ctl.s_free[1], (g1 - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
+        mma_commit_warp(&ctl.s_full[1]);
+        mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
+        if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
+        ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
+        for (int j = 0; ok && j < nkv1; ++j) {
+          const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
+          if (j + 1 < nkv0) {
+            ok = wait_full(ik) && wait(&ctl.s_free[0], (g0 + j) & 1);
+            if (!ok) break;
+            tc_fence_after();
             issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
             mma_commit_warp(&ctl.s_full[0]);
           }
+          ok = wait_full(iv);
+          if (ok && j < nkv0) {
+            ok = pv_halves(0, tO0, tP0, v_lo(iv), g0 + j, j);
+            if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
+          }
+          if (ok && j + 1 < nkv1) {
+            ok = wait_full(ik) && wait(&ctl.s_free[1], (g1 + j) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+            mma_commit_warp(&ctl.s_full[1]);
+            mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
+            if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
+          }
+          ok = ok && pv_halves(1, tO1, tP1, v_lo(iv), g1 + j, j);
+          if (!ok) break;
+          mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
+          if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
         }
-        ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j);
-        if (!ok) break;
-        mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
-        if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
-        if (more) {
-          issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
-          mma_commit_warp(&ctl.s_full[1]);
-          mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
-          if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
+      } else {
+        tc_fence_after();
+        issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
+        mma_commit_warp(&ctl.s_full[0]);
+        issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
+        mma_commit_warp(&ctl.s_full[1]);
+        mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
+        if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
+        // The unit's first P V overwrites O_0 and O_1: the previous unit's
+        // epilogue must have read them (waited here, outside the block loop).
+        ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
+        for (int j = 0; ok && j < nkv1; ++j) {
+          const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
+          const bool more = j + 1 < nkv1;
+          ok = wait_full(iv);
+          if (ok && j < nkv0) {
+            ok = pv_halves(0, tO0, tS0, v_lo(iv), g0 + j, j);
+            if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
+          }
+          if (ok && more) {
+            ok = wait_full(ik);
+            tc_fence_after();
+            if (ok && j + 1 < nkv0) {
+              issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
+              mma_commit_warp(&ctl.s_full[0]);
+            }
+          }
+          ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j);
+          if (!ok) break;
+          mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
+          if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
+          if (more) {
+            issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+            mma_commit_warp(&ctl.s_full[1]);
+            mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
+            if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
+          }
         }
       }
       it += 2 * nkv1;
@@ -618,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t tS = lane_base + t * kBM;
     const uint32_t tO = lane_base + C::kOCol + t * D;
+    const uint32_t tP = C::kSplitP ? lane_base + C::kPCol + t * 64 : tS;  // P_t
     const float cl2 = p.scale_log2;
     bool ok = true;
     uint32_t g = 0;  // key blocks done by this tile over all units of the block
@@ -663,7 +724,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_x32(tO + ch * 32, orr);
           }
         };
-        if (j == 0) {
+        // A bounded wait of the whole warp; false ends the block loop.
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+          bool good = mbar_wait(bar, parity, abort_flag, p.status, kStatusTimeoutSoftmax,
+                                p.wait_limit_ns);
+          good = __all_sync(0xffffffffu, good);
+          if (!good) ok = false;
+          return good;
+        };
+        if constexpr (C::kSplitP) {
+          // Split P: read all of S_t and hand its columns back to the MMA
+          // issuer at once; P_t goes to its own columns, each half once the
+          // previous block's P V has finished reading that half.
+          const uint32_t gj = g + j;
+          load_s(tS, lo, hi);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl.s_free[t]);
+          if (masked_block) {
+            mask_keys<0, 64>(lo, lim_blk);
+            mask_keys<64, 64>(hi, lim_blk);
+          }
+          if (j == 0) m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
+          if (gj > 0 && !wait_all(&ctl.pva_done[t], (gj - 1) & 1)) break;
+          float la = exp_keys_regs<BF16>(lo, cl2, m, tP);
+          // (the lazy-maximum test of the streaming path below, on registers)
+          bool check = j > 0 && la > p.two_pow_tau;
+          if (__any_sync(0xffffffffu, check)) {
+            const float bmax = row_max<64>(lo) * cl2;
+            const bool raise = check && bmax > m + p.tau;
+            if (__any_sync(0xffffffffu, raise)) {
+              // O_t must hold every earlier block before it is scaled
+              if (!wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
+              tc_fence_after();
+              const float alpha = raise ? ex2(m - bmax) : 1.f;
+              if (raise) m = bmax;
+              l *= alpha;
+              tmem_st_wait();
+              la = exp_keys_regs<BF16>(lo, cl2, m, tP);
+              rescale_o(alpha);
+            }
+          }
+          l += la;
+          release(0);
+          if (gj > 0 && !wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
+          float lb = exp_keys_regs<BF16>(hi, cl2, m, tP + 32);
+          check = j > 0 && lb > p.two_pow_tau;
+          if (__any_sync(0xffffffffu, check)) {
+            const float bmax = row_max<64>(hi) * cl2;
+            const bool raise = check && bmax > m + p.tau;
+            if (__any_sync(0xffffffffu, raise)) {
+              // keys 0-63 of this block are being multiplied into O_t
+              if (!wait_all(&ctl.pva_done[t], gj & 1)) break;
+              tc_fence_after();
+              const float alpha = raise ? ex2(m - bmax) : 1.f;
+              if (raise) m = bmax;
+              l *= alpha;
+              tmem_st_wait();
+              lb = exp_keys_regs<BF16>(hi, cl2, m, tP + 32);
+              rescale_o(alpha);
+            }
+          }
+          l += lb;
+          release(1);
+        } else if (j == 0) {
           // First block: no running maximum yet, so take the block maximum first.
           load_s(tS, lo, hi);
           if (masked_block) {
