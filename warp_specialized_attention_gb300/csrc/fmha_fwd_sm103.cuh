@@ -305,9 +305,11 @@ __device__ __forceinline__ void load_s(uint32_t tS, uint32_t (&lo)[64], uint32_t
   tmem_ld_wait_x32(d);
 }
 
-// Keys 0-63 of a block (two 32-column chunks of S into lo), exponentiated
-// against m as they arrive from TMEM; P to TMEM columns [0,32).  Starts the
-// load of keys 64-95 into hi before returning.  Returns the sum of P.
+// Keys 0-63 of a block: S columns 0-63 arrive in one TMEM round trip (two
+// 32-column loads, one wait; tcgen05.wait::ld waits for every outstanding
+// load), then the load of columns 64-95 into hi is put in flight and keys
+// 0-63 are exponentiated against m while it lands; P to TMEM columns [0,32).
+// Returns the sum of P.
 template <bool BF16>
 __device__ __forceinline__ float exp_keys_lo(uint32_t (&lo)[64], uint32_t (&hi)[64], uint32_t tS,
                                              uint64_t c2, uint64_t negm2, bool masked,
@@ -317,21 +319,20 @@ __device__ __forceinline__ float exp_keys_lo(uint32_t (&lo)[64], uint32_t (&hi)[
   uint32_t(&c2r)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
   uint32_t pk[16];
   tmem_ld_x32_async(tS, c0);
-  tmem_ld_wait_x32(c0);
   tmem_ld_x32_async(tS + 32, c1);
-  if (masked) mask_keys<0, 32>(c0, lim_blk);
-  float sum = exp_chunk<BF16>(c0, c2, negm2, pk);
-  tmem_st_x16_async(tS, pk);
+  tmem_ld_wait_x32(c0);
   tmem_ld_wait_x32(c1);
   tmem_ld_x32_async(tS + 64, c2r);
-  if (masked) mask_keys<32, 32>(c1, lim_blk);
+  if (masked) mask_keys<0, 64>(lo, lim_blk);
+  float sum = exp_chunk<BF16>(c0, c2, negm2, pk);
+  tmem_st_x16_async(tS, pk);
   sum += exp_chunk<BF16>(c1, c2, negm2, pk);
   tmem_st_x16_async(tS + 16, pk);
   return sum;
 }
 
-// Keys 64-127 (the first chunk's load already issued by exp_keys_lo); P to
-// TMEM columns [32,64).  Returns the sum of P.
+// Keys 64-127 (the load of 64-95 issued by exp_keys_lo; 96-127 follows it);
+// P to TMEM columns [32,64).  Returns the sum of P.
 template <bool BF16>
 __device__ __forceinline__ float exp_keys_hi(uint32_t (&hi)[64], uint32_t tS, uint64_t c2,
                                              uint64_t negm2, bool masked, int lim_blk) {
