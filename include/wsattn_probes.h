@@ -27,6 +27,15 @@ int wsa_probe_qk(const void* a, const void* b, float* c, int D, int bf16);
  * to the TMEM-operand form of tcgen05.mma; v is read as an MN-major operand. */
 int wsa_probe_pv(const void* p, const void* v, float* o, int D, int bf16);
 
+/* The 8-bit forms (tcgen05.mma.kind::f8f6f4, E4M3 operands, K = 32 per
+ * instruction) on one 128 x 128 x 128 tile:
+ *   c[128][128] = a[128][128] * b[128][128]^T           (both K-major, SMEM)
+ *   o[128][128] = p[128][128] * vt[128][128]^T           (p from TMEM, four
+ *                                                          values per column)
+ * a, b, p, vt: E4M3 bytes, row-major; vt is V transposed (vt[d][key]). */
+int wsa_probe_qk_e4m3(const void* a, const void* b, float* c);
+int wsa_probe_pv_e4m3(const void* p, const void* vt, float* o);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,6 +22,9 @@ def probes():
     for f in (lib.wsa_probe_qk, lib.wsa_probe_pv):
         f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int]
         f.restype = ctypes.c_int
+    for f in (lib.wsa_probe_qk_e4m3, lib.wsa_probe_pv_e4m3):
+        f.argtypes = [ctypes.c_void_p] * 3
+        f.restype = ctypes.c_int
     return lib
 
 
@@ -53,5 +56,35 @@ def test_pv_tile(probes, D, dtype):
     rc = probes.wsa_probe_pv(pd.data_ptr(), vd.data_ptr(), o.data_ptr(), D,
                              int(dtype == torch.bfloat16))
     assert rc == 0
+    err = (o.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err
+
+
+def _e4m3(x):
+    """E4M3 values (torch's float8_e4m3fn: max 448, no infinities) and their bytes."""
+    f8 = x.to(torch.float8_e4m3fn)
+    return f8.to(torch.float64), f8.view(torch.uint8).contiguous()
+
+
+def test_qk_tile_e4m3(probes):
+    g = torch.Generator().manual_seed(21)
+    a, a8 = _e4m3(torch.randn(128, 128, generator=g))
+    b, b8 = _e4m3(torch.randn(128, 128, generator=g))
+    ref = a @ b.T                      # products of E4M3 values are exact in fp32
+    c = torch.full((128, 128), float("nan"), device="cuda")
+    ad, bd = a8.cuda(), b8.cuda()
+    assert probes.wsa_probe_qk_e4m3(ad.data_ptr(), bd.data_ptr(), c.data_ptr()) == 0
+    err = (c.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err
+
+
+def test_pv_tile_e4m3(probes):
+    g = torch.Generator().manual_seed(23)
+    p, p8 = _e4m3(torch.rand(128, 128, generator=g) * 4)
+    v, v8 = _e4m3(torch.randn(128, 128, generator=g))
+    ref = p @ v
+    o = torch.full((128, 128), float("nan"), device="cuda")
+    pd, vtd = p8.cuda(), v8.T.contiguous().cuda()   # V goes in transposed: vt[d][key]
+    assert probes.wsa_probe_pv_e4m3(pd.data_ptr(), vtd.data_ptr(), o.data_ptr()) == 0
     err = (o.cpu().double() - ref).abs().max().item()
     assert err < 1e-3, "max abs error %g" % err
