@@ -321,8 +321,10 @@ def run_ours(args, w):
     torch.cuda.set_device(device)
     wsa.load_library()
 
-    q, k, v = synthetic.make_inputs_device(w, device, seed=rank_seed(w, rank))
-    o = torch.empty_like(q)
+    q, k, v_rows = synthetic.make_inputs_device(w, device, seed=rank_seed(w, rank))
+    fp8 = w.dtype == "e4m3"
+    v = synthetic.kernel_v(v_rows)           # E4M3 V goes in transposed, (B, H, D, S)
+    o = torch.empty(q.shape, device=device, dtype=torch.bfloat16 if fp8 else q.dtype)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -388,11 +390,15 @@ def run_ours(args, w):
 
     peaks, peak_src = _peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))  # fp16 dense peak equals bf16's
+    peak_note = "%s bf16 burst dense (fp16 nominal ratio 1)" % peak_src
+    if fp8:   # dense E4M3 runs at twice the 16-bit rate (4.5 vs 2.25 PFLOP/s nominal)
+        peak *= 2
+        peak_note = "%s bf16 burst dense x 2 (nominal e4m3/bf16 ratio)" % peak_src
     traffic = _traffic(w.name)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, q, k, v)
+        cpu = cpu_baseline(w, q, k, v_rows)
 
     if dist is not None:
         dist.destroy_process_group()
@@ -409,7 +415,7 @@ def run_ours(args, w):
                 "api": "fmha_fwd_host, pinned host buffers, %s chunks" % (args.chunks or 8)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": "%s bf16 burst dense (fp16 nominal ratio 1)" % peak_src,
+                     "peak_source": peak_note,
                      "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(launches)},
         "cpu_baseline": cpu,
         "clocks": clocks,
@@ -426,7 +432,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synthetic.HEADLINE.name,
-                    choices=[x.name for x in synthetic.WORKLOADS])
+                    choices=[x.name for x in synthetic.WORKLOADS + synthetic.FP8_WORKLOADS])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunks", type=int, default=0,
                     help="(batch, head) chunks for the end-to-end leg (0: library default)")

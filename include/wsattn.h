@@ -20,6 +20,16 @@
  *     LSE[b,h,i] = ln sum_{j in J_i} exp(s_ij)          (natural log)
  *
  * with fp32 accumulation; O is stored in the input dtype, LSE in fp32.
+ *
+ * FP8.  The same page times multi-head attention in FP8 as well as FP16
+ * (Section V-D, Fig. 10: sequence length 1024-16384, batch 4, head dim 128).
+ * With dtype FMHA_E4M3, Q, K and V hold E4M3 values (the OCP 8-bit format:
+ * 4 exponent bits, 3 mantissa bits, largest finite 448, no infinities), both
+ * products run on the 8-bit tensor-core path, P is rounded to E4M3 between
+ * the two stages, O is stored in bf16 and LSE in fp32.  The definition above
+ * applies to the E4M3 values as given; dequantisation scales are the
+ * caller's: fold the Q and K scales into `scale` and multiply O by V's scale
+ * (O is linear in V).
  */
 #ifndef WSATTN_H_
 #define WSATTN_H_
@@ -34,30 +44,36 @@ extern "C" {
 typedef enum {
   FMHA_OK = 0,
   FMHA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, non-finite or non-positive scale */
-  FMHA_ERR_UNSUPPORTED = 2, /* valid but not implemented: D not in {64, 128}, unknown dtype */
+  FMHA_ERR_UNSUPPORTED = 2, /* valid but not implemented: D not in {64, 128}, unknown dtype,
+                               E4M3 with D != 128 or S not a multiple of 16 */
   FMHA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (see fmha_last_cuda_error) */
   FMHA_ERR_TIMEOUT = 4      /* a device-side wait ran past its limit; outputs are undefined */
 } fmha_status;
 
-/* Element type of Q, K, V and O. */
-typedef enum { FMHA_F16 = 0, FMHA_BF16 = 1 } fmha_dtype;
+/* Element type of Q, K, V (and of O: the same, except bf16 for FMHA_E4M3). */
+typedef enum { FMHA_F16 = 0, FMHA_BF16 = 1, FMHA_E4M3 = 2 } fmha_dtype;
 
 /*
  * fmha_fwd -- fused attention forward pass, O and LSE, on one GPU.
  *
  *   q, k, v  device pointers, each B*H*S*D elements of `dtype`, contiguous
  *            (B, H, S, D): element (b,h,s,d) at ((b*H + h)*S + s)*D + d.
- *            Read only.  16-byte aligned.
- *   o        device pointer, B*H*S*D elements of `dtype`, same layout.  Written.
- *            16-byte aligned; must not overlap q, k, v or lse.
+ *            Read only.  16-byte aligned.  For FMHA_E4M3, v holds V
+ *            transposed per (batch, head), contiguous (B, H, D, S): element
+ *            (b,h,s,d) of V at ((b*H + h)*D + d)*S + s.
+ *   o        device pointer, B*H*S*D elements of `dtype` (bf16 for FMHA_E4M3),
+ *            (B, H, S, D) layout.  Written.  16-byte aligned; must not overlap
+ *            q, k, v or lse.
  *   lse      device pointer, B*H*S fp32, contiguous (B, H, S).  Written.
  *            4-byte aligned.
  *   B, H, S  batch, heads, sequence length (queries = keys), each >= 1;
  *            B*H < 2^31 and ceil(S/256)*B*H < 2^31.
- *   D        head dimension: 64 or 128 (anything else -> FMHA_ERR_UNSUPPORTED).
+ *   D        head dimension: 64 or 128 (anything else -> FMHA_ERR_UNSUPPORTED);
+ *            128 for FMHA_E4M3, which also needs S % 16 == 0 (the rows of the
+ *            transposed V must start on 16-byte boundaries).
  *   causal   0: every key visible; nonzero: key j visible to query i iff j <= i.
  *   scale    softmax scale applied to q.k, finite and > 0 (usually 1/sqrt(D)).
- *   dtype    FMHA_F16 or FMHA_BF16.
+ *   dtype    FMHA_F16, FMHA_BF16 or FMHA_E4M3.
  *   stream   cudaStream_t (as void*) on which the kernel is enqueued; NULL is the
  *            legacy default stream.  Must belong to the current device, which
  *            must hold all five buffers.
@@ -80,7 +96,8 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
  * fmha_fwd_host -- fmha_fwd on host-resident tensors, with the host<->device
  * transfers overlapped with the computation.
  *
- *   q, k, v    host pointers, B*H*S*D elements of `dtype`, (B, H, S, D) layout.
+ *   q, k, v    host pointers, B*H*S*D elements of `dtype`, in fmha_fwd's
+ *              layouts (v transposed per head for FMHA_E4M3).
  *              Page-locked (pinned) memory lets the copies run asynchronously
  *              and overlap; pageable memory works but serialises them.
  *   o, lse     host pointers, outputs in the same layouts as fmha_fwd.

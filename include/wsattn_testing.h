@@ -28,9 +28,11 @@ extern "C" {
  *                    Outputs are undefined.
  *   wait_limit_s  per-wait time limit in seconds, in (0, 60]; fmha_fwd uses 1.
  *   tau           lazy-rescale threshold of the online softmax in log2 units,
- *                 in [0, 15]; fmha_fwd uses 15.  The running maximum is raised
- *                 (and O rescaled) only when a block's maximum exceeds it by more
- *                 than tau, so P <= 2^tau (15 keeps P inside the f16 range).  The
+ *                 in [0, 15] ([0, 8] for FMHA_E4M3); fmha_fwd uses 15 (8 for
+ *                 FMHA_E4M3).  The running maximum is raised (and O rescaled)
+ *                 only when a block's maximum exceeds it by more than tau, so
+ *                 P <= 2^tau (15 keeps P inside the f16 range; E4M3 P is
+ *                 stored as 2^(8-tau) P <= 256, inside its range of 448).  The
  *                 result does not depend on tau; 0 gives the classic online
  *                 softmax that rescales whenever the maximum grows.
  *

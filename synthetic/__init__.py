@@ -33,7 +33,7 @@ class Workload:
     H: int
     S: int
     D: int
-    dtype: str          # "f16" or "bf16"
+    dtype: str          # "f16", "bf16" or "e4m3" (E4M3 Q, K, V; O in bf16)
     causal: bool
     k_mult: float = 1.0
     seed: int = 0
@@ -45,7 +45,8 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+        return {"f16": torch.float16, "bf16": torch.bfloat16,
+                "e4m3": torch.float8_e4m3fn}[self.dtype]
 
     @property
     def flops(self) -> float:
@@ -69,12 +70,26 @@ WORKLOADS = [
 ]
 HEADLINE = WORKLOADS[4]
 
+# The headline shape with E4M3 inputs: a benchmark and parity line for the
+# 8-bit path, not one of the five contract configurations above.
+FP8_WORKLOADS = [
+    Workload("b4h32s16k_d128_e4m3", 4, 32, 16384, 128, "e4m3", False, 1.0, 1104),
+]
+
 
 def by_name(name: str) -> Workload:
-    for w in WORKLOADS:
+    for w in WORKLOADS + FP8_WORKLOADS:
         if w.name == name:
             return w
     raise KeyError(name)
+
+
+def _scale(t: torch.Tensor, f: float) -> torch.Tensor:
+    """t * f in t's dtype (exact for the power-of-two factors used here);
+    float8 has no arithmetic of its own, so it goes through float32."""
+    if t.dtype == torch.float8_e4m3fn:
+        return (t.float() * f).to(t.dtype)
+    return t * f
 
 
 def make_inputs(w: Workload, B=None, H=None, S=None, D=None, dtype=None, seed=None):
@@ -94,7 +109,7 @@ def make_inputs(w: Workload, B=None, H=None, S=None, D=None, dtype=None, seed=No
     k = torch.randn(B, H, S, D, generator=g, dtype=torch.float32).to(dt)
     v = torch.randn(B, H, S, D, generator=g, dtype=torch.float32).to(dt)
     if w.k_mult != 1.0:
-        k = k * w.k_mult
+        k = _scale(k, w.k_mult)
     return q.contiguous(), k.contiguous(), v.contiguous()
 
 
@@ -110,5 +125,13 @@ def make_inputs_device(w: Workload, device, seed=None):
                                dtype=torch.float32).to(w.torch_dtype))
     q, k, v = out
     if w.k_mult != 1.0:
-        k = k * w.k_mult
+        k = _scale(k, w.k_mult)
     return q, k, v
+
+
+def kernel_v(v: torch.Tensor) -> torch.Tensor:
+    """V in the layout the kernel takes for its dtype: (B, H, S, D) for 16-bit
+    inputs, transposed to (B, H, D, S) for E4M3."""
+    if v.dtype == torch.float8_e4m3fn:
+        return v.transpose(-1, -2).contiguous()
+    return v

@@ -73,6 +73,9 @@ def _call(lib, ptrs=None, B=1, H=1, S=128, D=128, causal=0, scale=0.088, dtype=0
     (dict(D=96), wsa.FMHA_ERR_UNSUPPORTED),
     (dict(D=256), wsa.FMHA_ERR_UNSUPPORTED),
     (dict(dtype=7), wsa.FMHA_ERR_UNSUPPORTED),
+    (dict(dtype=wsa.FMHA_E4M3, D=64), wsa.FMHA_ERR_UNSUPPORTED),     # E4M3: D = 128 only
+    (dict(dtype=wsa.FMHA_E4M3, S=1000), wsa.FMHA_ERR_UNSUPPORTED),   # transposed V rows: S % 16
+    (dict(dtype=wsa.FMHA_E4M3, scale=0.0), wsa.FMHA_ERR_INVALID_ARG),
     (dict(scale=0.0), wsa.FMHA_ERR_INVALID_ARG),
     (dict(scale=-0.1), wsa.FMHA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), wsa.FMHA_ERR_INVALID_ARG),
@@ -137,6 +140,21 @@ def test_testing_hook_rejects_bad_knobs(lib):
     assert lib.fmha_fwd_testing(*args, 0, 1.0, -1.0) == wsa.FMHA_ERR_INVALID_ARG
     assert lib.fmha_fwd_testing(*args, 0, 1.0, 16.0) == wsa.FMHA_ERR_INVALID_ARG
     assert lib.fmha_fwd_testing(*args, 0, 1.0, float("nan")) == wsa.FMHA_ERR_INVALID_ARG
+    # E4M3 P is stored as 2^(8 - tau) * P: tau above 8 would overflow it
+    args8 = (q, k, v, o, lse, 1, 1, 128, 128, 0, 0.088, wsa.FMHA_E4M3, None)
+    assert lib.fmha_fwd_testing(*args8, 0, 1.0, 8.5) == wsa.FMHA_ERR_INVALID_ARG
+
+
+def test_e4m3_overlap_uses_the_byte_sizes(lib):
+    """Inputs are 1 byte per element and O 2 bytes: an O that starts inside
+    the second half of a same-count 16-bit-sized region of q is still past q's
+    E4M3 bytes, so it is accepted up to validation (a CUDA error here, no GPU);
+    one that starts inside q's bytes is rejected."""
+    q, k, v, o, lse = _ptrs()
+    n = 1 * 1 * 128 * 128
+    assert _call(lib, [q, k, v, q + n - 16, lse], dtype=wsa.FMHA_E4M3) == wsa.FMHA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert _call(lib, [q, k, v, q + n, lse], dtype=wsa.FMHA_E4M3) == wsa.FMHA_ERR_CUDA
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")

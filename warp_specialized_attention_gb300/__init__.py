@@ -23,13 +23,13 @@ import torch
 
 __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
-    "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FmhaError", "LibraryNotBuilt",
+    "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
     "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
     "get_device_status", "status_str", "version",
 ]
 
 FMHA_OK, FMHA_ERR_INVALID_ARG, FMHA_ERR_UNSUPPORTED, FMHA_ERR_CUDA, FMHA_ERR_TIMEOUT = range(5)
-FMHA_F16, FMHA_BF16 = 0, 1
+FMHA_F16, FMHA_BF16, FMHA_E4M3 = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libwsattn.so")
@@ -103,7 +103,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return FMHA_F16
     if t.dtype == torch.bfloat16:
         return FMHA_BF16
-    raise TypeError("q/k/v must be float16 or bfloat16, got %s" % t.dtype)
+    if t.dtype == torch.float8_e4m3fn:
+        return FMHA_E4M3
+    raise TypeError("q/k/v must be float16, bfloat16 or float8_e4m3fn, got %s" % t.dtype)
 
 
 def _stream_handle(stream) -> int:
@@ -122,10 +124,15 @@ def _check(q, k, v, o, lse):
             raise ValueError("%s must be a CUDA tensor" % name)
         if not t.is_contiguous():
             raise ValueError("%s must be contiguous" % name)
-    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape or q.shape != o.shape:
-        raise ValueError("q, k, v, o must share one (B, H, S, D) shape")
-    if not (q.dtype == k.dtype == v.dtype == o.dtype):
-        raise TypeError("q, k, v, o must share one dtype")
+    fp8 = q.dtype == torch.float8_e4m3fn
+    if q.dim() != 4 or q.shape != k.shape or q.shape != o.shape:
+        raise ValueError("q, k, o must share one (B, H, S, D) shape")
+    B, H, S, D = q.shape
+    if tuple(v.shape) != ((B, H, D, S) if fp8 else (B, H, S, D)):
+        raise ValueError("v must be (B, H, S, D), or (B, H, D, S) (transposed) for float8_e4m3fn")
+    if not (q.dtype == k.dtype == v.dtype) or o.dtype != (torch.bfloat16 if fp8 else q.dtype):
+        raise TypeError("q, k, v must share one dtype; o has it too, or is bfloat16 for "
+                        "float8_e4m3fn inputs")
     if lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q.shape[:3]):
         raise ValueError("lse must be float32 of shape (B, H, S)")
     devs = {t.device for t in (q, k, v, o, lse)}
@@ -138,8 +145,10 @@ def fmha_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
     """Enqueue the forward kernel: o, lse <- attention(q, k, v).
 
     q, k, v, o: contiguous (B, H, S, D) CUDA tensors of one dtype (f16/bf16);
-    lse: contiguous (B, H, S) float32.  scale defaults to the float32 value
-    of 1/sqrt(D).  Asynchronous on ``stream`` (default: torch's current stream).
+    or q, k float8_e4m3fn (B, H, S, D), v float8_e4m3fn transposed (B, H, D, S)
+    and o bfloat16 (B, H, S, D).  lse: contiguous (B, H, S) float32.  scale
+    defaults to the float32 value of 1/sqrt(D).  Asynchronous on ``stream``
+    (default: torch's current stream).
     """
     lib = load_library()
     _check(q, k, v, o, lse)
@@ -203,8 +212,11 @@ def get_device_status(stream=None, device=None) -> int:
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Allocate O (dtype of q) and LSE (float32) with torch and run fmha_fwd."""
-    o = torch.empty_like(q)
+    """Allocate O (dtype of q; bfloat16 for float8_e4m3fn inputs) and LSE
+    (float32) with torch and run fmha_fwd.  For float8_e4m3fn, v is given
+    transposed, (B, H, D, S)."""
+    o = torch.empty(q.shape, device=q.device,
+                    dtype=torch.bfloat16 if q.dtype == torch.float8_e4m3fn else q.dtype)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     fmha_fwd(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
     return o, lse

@@ -27,7 +27,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + INCLUDE, "-I" + CSRC]
 
-LIB_UNITS = ["fmha_api.cu", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu"]
+LIB_UNITS = ["fmha_api.cu", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu", "fmha_fwd_e4m3.cu"]
 PROBE_UNITS = ["probes.cu"]
 HEADERS = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_launch.h"]
 

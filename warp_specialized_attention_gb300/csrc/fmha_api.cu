@@ -61,23 +61,31 @@ EncodeTiledFn encode_fn(cudaError_t* err) {
   return fn;
 }
 
-// (B*H, S, D) 16-bit tensor viewed as a 3-D map, box = 64 elements (128 bytes)
-// x 128 rows x 1 head, 128-byte swizzle.  Rows past S read as zeros.
-bool encode_bhsd(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, bool bf16, int64_t BH,
-                 int64_t S, int64_t D) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+// (B*H, rows, cols) tensor viewed as a 3-D map: box = 128 bytes of a row
+// (64 16-bit or 128 8-bit elements) x 128 rows x 1 head, 128-byte swizzle.
+// Rows past the end read as zeros.  Q, K, V: rows = S, cols = D; the
+// transposed E4M3 V: rows = D, cols = S.
+bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype, int64_t BH,
+                int64_t rows, int64_t cols) {
+  const int64_t eb = dtype == FMHA_E4M3 ? 1 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2),
-                                 static_cast<cuuint64_t>(S * D * 2)};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * eb),
+                                 static_cast<cuuint64_t>(rows * cols * eb)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r =
-      enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType t = dtype == FMHA_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                : dtype == FMHA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = enc(map, t, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+// Bytes per element of the inputs and of O.
+size_t in_bytes(int dtype) { return dtype == FMHA_E4M3 ? 1 : 2; }
+constexpr size_t kOutBytes = 2;
 
 // Device address of the status word, looked up once per device.
 cudaError_t status_word(int** out) {
@@ -118,36 +126,37 @@ fmha_status validate(const void* q, const void* k, const void* v, void* o, float
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S < 1 || D < 1) return FMHA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FMHA_ERR_INVALID_ARG;
-  if (dtype != FMHA_F16 && dtype != FMHA_BF16) return FMHA_ERR_UNSUPPORTED;
+  if (dtype != FMHA_F16 && dtype != FMHA_BF16 && dtype != FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return FMHA_ERR_UNSUPPORTED;
+  if (dtype == FMHA_E4M3 && (D != 128 || S % 16 != 0)) return FMHA_ERR_UNSUPPORTED;
   const int64_t lim = (int64_t{1} << 31) - 1;
   if (B > lim || H > lim || S > lim || B * H > lim) return FMHA_ERR_INVALID_ARG;
   const int64_t nq = (S + 255) / 256;
   if (nq * B * H > lim) return FMHA_ERR_INVALID_ARG;
   const size_t n = static_cast<size_t>(B * H) * static_cast<size_t>(S) * static_cast<size_t>(D);
-  const size_t ob = n * 2, lb = static_cast<size_t>(B * H * S) * 4;
-  if (overlaps(o, ob, q, ob) || overlaps(o, ob, k, ob) || overlaps(o, ob, v, ob) ||
-      overlaps(o, ob, lse, lb) || overlaps(lse, lb, q, ob) || overlaps(lse, lb, k, ob) ||
-      overlaps(lse, lb, v, ob))
+  const size_t ib = n * in_bytes(dtype), ob = n * kOutBytes;
+  const size_t lb = static_cast<size_t>(B * H * S) * 4;
+  if (overlaps(o, ob, q, ib) || overlaps(o, ob, k, ib) || overlaps(o, ob, v, ib) ||
+      overlaps(o, ob, lse, lb) || overlaps(lse, lb, q, ib) || overlaps(lse, lb, k, ib) ||
+      overlaps(lse, lb, v, ib))
     return FMHA_ERR_INVALID_ARG;
   return FMHA_OK;
 }
 
 fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
-                     void* stream, int inject, uint64_t wait_limit_ns,
-                     float tau = wsa::kTauDefault) {
+                     void* stream, int inject, uint64_t wait_limit_ns, float tau = -1.f) {
   const fmha_status vs = validate(q, k, v, o, lse, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
 
   cudaError_t e;
   EncodeTiledFn enc = encode_fn(&e);
   if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
-  const bool bf16 = dtype == FMHA_BF16;
+  const bool bf16 = dtype == FMHA_BF16, e4m3 = dtype == FMHA_E4M3;
   const int64_t BH = B * H;
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!encode_bhsd(enc, &tq, q, bf16, BH, S, D) || !encode_bhsd(enc, &tk, k, bf16, BH, S, D) ||
-      !encode_bhsd(enc, &tv, v, bf16, BH, S, D))
+  if (!encode_map(enc, &tq, q, dtype, BH, S, D) || !encode_map(enc, &tk, k, dtype, BH, S, D) ||
+      !(e4m3 ? encode_map(enc, &tv, v, dtype, BH, D, S) : encode_map(enc, &tv, v, dtype, BH, S, D)))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
 
   int* status = nullptr;
@@ -166,13 +175,20 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = wait_limit_ns;
   prm.inject = inject;
+  // E4M3 P is stored scaled by 2^(8 - tau), so its largest value is 256 < 448.
+  // The default tau = 8 (scale 1) redoes blocks as rarely as the E4M3 range
+  // allows; tau = 0 (scale 2^8) keeps smaller P out of the subnormal range at
+  // the cost of an exact maximum on nearly every block (1.7x slower).
+  if (tau < 0.f) tau = e4m3 ? wsa::kTauDefaultE4m3 : wsa::kTauDefault;
   prm.tau = tau;
-  prm.two_pow_tau = std::exp2(tau);
+  prm.p_shift = e4m3 ? 8.f - tau : 0.f;
+  prm.two_pow_tau = std::exp2(tau + prm.p_shift);
   const unsigned grid = static_cast<unsigned>(prm.n_qblk * BH);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  e = D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, prm, grid, st)
-              : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, prm, grid, st);
+  e = e4m3      ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, prm, grid, st)
+      : D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, prm, grid, st)
+                : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, prm, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return FMHA_OK;
 }
@@ -220,11 +236,14 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
   const fmha_status vs = validate(dq, dk, dv, d_o, dlse, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
   const int64_t BH = B * H;
-  const size_t slice = static_cast<size_t>(S * D * 2), lslice = static_cast<size_t>(S) * 4;
-  const size_t host_bytes = static_cast<size_t>(BH) * slice;
-  if (overlaps(q, host_bytes, o, host_bytes) || overlaps(k, host_bytes, o, host_bytes) ||
-      overlaps(v, host_bytes, o, host_bytes) ||
-      overlaps(lse, static_cast<size_t>(BH) * lslice, o, host_bytes))
+  // one (batch, head) slice of an input, of O and of LSE (V's transposed E4M3
+  // slice has the same size as the others)
+  const size_t slice = static_cast<size_t>(S * D) * in_bytes(dtype);
+  const size_t oslice = static_cast<size_t>(S * D) * kOutBytes, lslice = static_cast<size_t>(S) * 4;
+  const size_t in_host = static_cast<size_t>(BH) * slice, o_host = static_cast<size_t>(BH) * oslice;
+  if (overlaps(q, in_host, o, o_host) || overlaps(k, in_host, o, o_host) ||
+      overlaps(v, in_host, o, o_host) ||
+      overlaps(lse, static_cast<size_t>(BH) * lslice, o, o_host))
     return FMHA_ERR_INVALID_ARG;
   const int64_t chunks = std::min<int64_t>(n_chunks == 0 ? 8 : n_chunks, BH);
 
@@ -244,6 +263,7 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
   for (int64_t c = 0; c < chunks; ++c) {
     const int64_t s0 = BH * c / chunks, s1 = BH * (c + 1) / chunks, n = s1 - s0;
     const size_t off = static_cast<size_t>(s0) * slice, bytes = static_cast<size_t>(n) * slice;
+    const size_t ooff = static_cast<size_t>(s0) * oslice, obytes = static_cast<size_t>(n) * oslice;
     const size_t loff = static_cast<size_t>(s0) * lslice, lbytes = static_cast<size_t>(n) * lslice;
     if ((e = cudaMemcpyAsync(at(dq, off), at(q, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
             cudaSuccess ||
@@ -256,13 +276,13 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
       return cuda_fail(e, "host-to-device copy");
     // one (batch, head) range is a B = 1, H = n problem at offset pointers
     const fmha_status ks =
-        fwd_impl(at(dq, off), at(dk, off), at(dv, off), at(d_o, off),
+        fwd_impl(at(dq, off), at(dk, off), at(dv, off), at(d_o, ooff),
                  static_cast<float*>(at(dlse, loff)), 1, n, S, D, causal, scale, dtype, stream, 0,
                  kDefaultWaitLimitNs);
     if (ks != FMHA_OK) return ks;
     if ((e = cudaEventRecord(hp->computed[c], st)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(at(o, off), at(d_o, off), bytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
+        (e = cudaMemcpyAsync(at(o, ooff), at(d_o, ooff), obytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
             cudaSuccess ||
         (e = cudaMemcpyAsync(at(lse, loff), at(dlse, loff), lbytes, cudaMemcpyDeviceToHost,
                              hp->d2h)) != cudaSuccess)
@@ -292,7 +312,7 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
                              double wait_limit_s, float tau) {
   if (inject_fault < 0 || inject_fault > 1) return FMHA_ERR_INVALID_ARG;
   if (!(wait_limit_s > 0.0) || wait_limit_s > 60.0) return FMHA_ERR_INVALID_ARG;
-  if (!(tau >= 0.f && tau <= 15.f)) return FMHA_ERR_INVALID_ARG;
+  if (!(tau >= 0.f && tau <= (dtype == FMHA_E4M3 ? 8.f : 15.f))) return FMHA_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream,
                   inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9), tau);
 }

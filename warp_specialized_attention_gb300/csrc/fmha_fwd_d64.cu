@@ -8,10 +8,10 @@ cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap& tq, const 
                            const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
                            cudaStream_t stream) {
   if (bf16)
-    return causal ? launch_fmha_fwd<64, true, true>(tq, tk, tv, prm, grid, stream)
-                  : launch_fmha_fwd<64, true, false>(tq, tk, tv, prm, grid, stream);
-  return causal ? launch_fmha_fwd<64, false, true>(tq, tk, tv, prm, grid, stream)
-                : launch_fmha_fwd<64, false, false>(tq, tk, tv, prm, grid, stream);
+    return causal ? launch_fmha_fwd<64, kBF16, true>(tq, tk, tv, prm, grid, stream)
+                  : launch_fmha_fwd<64, kBF16, false>(tq, tk, tv, prm, grid, stream);
+  return causal ? launch_fmha_fwd<64, kF16, true>(tq, tk, tv, prm, grid, stream)
+                : launch_fmha_fwd<64, kF16, false>(tq, tk, tv, prm, grid, stream);
 }
 
 }  // namespace wsa

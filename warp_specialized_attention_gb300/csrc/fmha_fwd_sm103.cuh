@@ -81,8 +81,13 @@ constexpr int kBN = 128;       // keys per block
 constexpr int kThreads = 320;  // 10 warps
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
-constexpr float kTauDefault = 15.0f;  // lazy-rescale threshold, log2 units
+constexpr float kTauDefault = 15.0f;     // lazy-rescale threshold, log2 units (16-bit P)
+constexpr float kTauDefaultE4m3 = 8.0f;  // E4M3 P: stored unscaled, <= 2^8 = 256 < 448
 constexpr uint32_t kTmemCols = 512;
+
+// Element types: Q, K, V (and P, O) in f16 or bf16; or E4M3 Q, K, V (V
+// supplied transposed per head), P in E4M3 and O in bf16.
+enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 
 // Device status bits (OR-ed into the status word on an abandoned wait).
 enum : int {
@@ -92,12 +97,16 @@ enum : int {
   kStatusTimeoutDrain = 8,
 };
 
-template <int D>
+template <int D, int ET>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring slots
-  static constexpr int kTileBytes = kBM * D * 2;          // 128 x D 16-bit
-  static constexpr int kSlotBytes = kBN * D * 2;
+  static_assert(ET != kE4M3 || D == 128, "E4M3 inputs: head dim 128");
+  static constexpr int kElemBytes = ET == kE4M3 ? 1 : 2;
+  static constexpr int kTileBytes = kBM * D * kElemBytes;  // 128 x D
+  static constexpr int kSlotBytes = kBN * D * kElemBytes;
+  static constexpr int kStages = kSlotBytes == 16384 ? 8 : 4;  // K/V ring slots
+  static constexpr int kBoxElems = 128 / kElemBytes;       // elements per 128-byte row of a box
+  static constexpr int kColBlocks = D * kElemBytes / 128;  // 128-byte column blocks of a row
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingOff = kQBytes;
   static constexpr int kCtlOff = kRingOff + kStages * kSlotBytes;
@@ -105,7 +114,7 @@ struct Cfg {
   static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
   // D = 64 leaves 128 TMEM columns free: P_t gets its own 64 columns there
   // (split P), so S_t can be overwritten as soon as the softmax has read it.
-  static constexpr bool kSplitP = D == 64;
+  static constexpr bool kSplitP = D == 64 && ET != kE4M3;
   static constexpr uint32_t kPCol = 256 + 2 * D;           // split P_t at kPCol + 64t
   static_assert(!kSplitP || kPCol + 128 <= 512, "TMEM columns");
 };
@@ -146,7 +155,11 @@ struct FwdParams {
   uint64_t wait_limit_ns;
   int inject;         // 0 in normal use; 1 drops one softmax arrival (timeout test)
   float tau;          // lazy-rescale threshold (log2 units), 0 <= tau <= 15
-  float two_pow_tau;  // 2^tau
+  float two_pow_tau;  // 2^(tau + p_shift): the half-sum that proves no raise is due
+  float p_shift;      // P is stored as 2^p_shift * exp2(s*c - m): 0 for 16-bit P;
+                      // 8 - tau for E4M3, so P <= 256 < 448 and small P stay
+                      // out of the E4M3 subnormal range (l carries the same
+                      // factor, so O = P V / l is unchanged)
 };
 
 // A work unit: one (batch*head) index and one 256-row query block.
@@ -183,45 +196,63 @@ __device__ __forceinline__ Unit decode_unit(int x, const FwdParams& p) {
 
 // Shared-memory operand descriptors, 128-byte swizzle.  High half: 8-row groups
 // 1024 bytes apart.  Low half: start address plus the leading byte offset,
-// which K-major operands (Q, K: rows of 64 elements) do not use and the
-// MN-major V operand of P V uses as the distance between its 64-column blocks.
+// which K-major operands (Q, K and the transposed 8-bit V: rows of 128 bytes)
+// do not use and the MN-major 16-bit V operand of P V uses as the distance
+// between its 64-column blocks.
 constexpr uint32_t kDescHi = sdesc_hi(1024);
 constexpr uint32_t kLboKMajor = 16;
 constexpr uint32_t kLboV = kBN * 128;
 
-// S = Q K^T into TMEM, D/16 steps of K = 16 (32 bytes within a 128-byte row;
-// every fourth step moves to the next 16 KB column block).  Warp-collective.
-template <int D, bool BF16>
+// S = Q K^T into TMEM: D / K steps of K = 16 (16-bit) or 32 (E4M3) elements,
+// 32 bytes within a 128-byte row; every fourth step moves to the next 16 KB
+// column block.  Warp-collective.
+template <int D, int ET>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
   static_assert(kBM == kBN, "Q and K tiles share one column-block size");
-  constexpr uint32_t idesc = idesc_f16(BF16, kBM, kBN, false);
+  constexpr int kStep = ET == kE4M3 ? 32 : 16;
+  constexpr uint32_t idesc = idesc_f16(ET == kBF16, kBM, kBN, false);
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < D / kStep; ++kk) {
     const uint32_t step = (kk >> 2) * ((kBM * 128) >> 4) + (kk & 3) * (32 >> 4);
-    mma_ss_warp(d_tmem, sdesc_join(q_lo + step, kDescHi), sdesc_join(k_lo + step, kDescHi), idesc,
-                kk > 0 ? 1u : 0u);
+    const uint64_t a = sdesc_join(q_lo + step, kDescHi), b = sdesc_join(k_lo + step, kDescHi);
+    if constexpr (ET == kE4M3)
+      mma_ss_f8_warp(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    else
+      mma_ss_warp(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O (+)= P V over keys [64*half, 64*half + 64): P from TMEM (16 keys = 8
-// columns per step), V rows 16 at a time.  Warp-collective.
-template <int D, bool BF16>
+// O (+)= P V over keys [64*half, 64*half + 64), P from TMEM (8 columns per
+// step).  16-bit: 16 keys per step, V MN-major, 16 rows (2 KB) per step.
+// E4M3: 32 keys per step, V transposed (K-major, 128 keys per 128-byte row),
+// 32 bytes along the row per step.  Warp-collective.
+template <int D, int ET>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                               int half, bool accumulate) {
-  constexpr uint32_t idesc = idesc_f16(BF16, kBM, D, true);
+  if constexpr (ET == kE4M3) {
+    constexpr uint32_t idesc = idesc_f16(false, kBM, D, false);
 #pragma unroll
-  for (int k4 = 0; k4 < 4; ++k4) {
-    const int kk = half * 4 + k4;
-    mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * ((16 * 128) >> 4), kDescHi),
-                idesc, (accumulate || kk > 0) ? 1u : 0u);
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int kk = half * 2 + k2;
+      mma_ts_f8_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * (32 >> 4), kDescHi), idesc,
+                     (accumulate || kk > 0) ? 1u : 0u);
+    }
+  } else {
+    constexpr uint32_t idesc = idesc_f16(ET == kBF16, kBM, D, true);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int kk = half * 4 + k4;
+      mma_ts_warp(d_tmem, p_tmem + kk * 8, sdesc_join(v_lo + kk * ((16 * 128) >> 4), kDescHi),
+                  idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
   }
 }
 
-template <int D, bool BF16>
+template <int D, int ET>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                          bool accumulate) {
-  issue_pv_half<D, BF16>(d_tmem, p_tmem, v_lo, 0, accumulate);
-  issue_pv_half<D, BF16>(d_tmem, p_tmem, v_lo, 1, true);
+  issue_pv_half<D, ET>(d_tmem, p_tmem, v_lo, 0, accumulate);
+  issue_pv_half<D, ET>(d_tmem, p_tmem, v_lo, 1, true);
 }
 
 // Raw S values (fp32 bit patterns) of keys with in-block index >= lim_blk
@@ -244,12 +275,14 @@ __device__ __forceinline__ float row_max(const uint32_t* s) {
   return fmaxf(fmaxf(a, b), fmaxf(__uint_as_float(s[N - 2]), __uint_as_float(s[N - 1])));
 }
 
-// P for 32 keys: p = exp2(s*c - m), rounded pairwise to 16 bits into pk; returns
+// P for 32 keys: p = exp2(s*c - m), rounded to the P type and packed into pk
+// (16-bit: two per word, pk[0..15]; E4M3: four per word, pk[0..7]); returns
 // the fp32 sum of the 32 values.
-template <bool BF16>
+template <int ET>
 __device__ __forceinline__ float exp_chunk(const uint32_t* s, uint64_t c2, uint64_t negm2,
                                            uint32_t (&pk)[16]) {
   uint64_t acc0 = 0, acc1 = 0;
+  float prev_a = 0.f, prev_b = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint64_t x = ffma2(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])),
@@ -262,7 +295,14 @@ __device__ __forceinline__ float exp_chunk(const uint32_t* s, uint64_t c2, uint6
       acc1 = fadd2(acc1, f2_pack(a, b));
     else
       acc0 = fadd2(acc0, f2_pack(a, b));
-    pk[i] = pack2<BF16>(a, b);
+    if constexpr (ET == kE4M3) {
+      if (i & 1)
+        pk[i >> 1] = pack4_e4m3(prev_a, prev_b, a, b);
+      prev_a = a;
+      prev_b = b;
+    } else {
+      pk[i] = pack2<ET == kBF16>(a, b);
+    }
   }
   float s0, s1, s2, s3;
   f2_unpack(acc0, s0, s1);
@@ -270,23 +310,18 @@ __device__ __forceinline__ float exp_chunk(const uint32_t* s, uint64_t c2, uint6
   return (s0 + s1) + (s2 + s3);
 }
 
-// P for a whole block already in registers (keys 0-63 in lo, 64-127 in hi);
-// stores it over the first 64 TMEM columns of S (no wait).  Returns the sum.
-template <bool BF16>
-__device__ __forceinline__ float exp_block(const uint32_t* lo, const uint32_t* hi, float cl2,
-                                           float m, uint32_t tS) {
-  const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
-  float sum = 0.f;
-  uint32_t pk[16];
-  sum += exp_chunk<BF16>(lo, c2, negm2, pk);
-  tmem_st_x16_async(tS, pk);
-  sum += exp_chunk<BF16>(lo + 32, c2, negm2, pk);
-  tmem_st_x16_async(tS + 16, pk);
-  sum += exp_chunk<BF16>(hi, c2, negm2, pk);
-  tmem_st_x16_async(tS + 32, pk);
-  sum += exp_chunk<BF16>(hi + 32, c2, negm2, pk);
-  tmem_st_x16_async(tS + 48, pk);
-  return sum;
+// TMEM columns P takes per 32 keys: 16 (16-bit) or 8 (E4M3).
+template <int ET>
+constexpr uint32_t kPColsPer32 = ET == kE4M3 ? 8u : 16u;
+
+// Stores the P of 32-key chunk `chunk` of a block at its columns from tP (no
+// wait).
+template <int ET>
+__device__ __forceinline__ void store_p(uint32_t tP, int chunk, const uint32_t (&pk)[16]) {
+  if constexpr (ET == kE4M3)
+    tmem_st_x8_async(tP + chunk * kPColsPer32<ET>, pk);
+  else
+    tmem_st_x16_async(tP + chunk * kPColsPer32<ET>, pk);
 }
 
 // Loads keys 0-63 of S into lo and 64-127 into hi (waits).
@@ -308,9 +343,9 @@ __device__ __forceinline__ void load_s(uint32_t tS, uint32_t (&lo)[64], uint32_t
 // Keys 0-63 of a block: S columns 0-63 arrive in one TMEM round trip (two
 // 32-column loads, one wait; tcgen05.wait::ld waits for every outstanding
 // load), then the load of columns 64-95 into hi is put in flight and keys
-// 0-63 are exponentiated against m while it lands; P to TMEM columns [0,32).
-// Returns the sum of P.
-template <bool BF16>
+// 0-63 are exponentiated against m while it lands; P over the first S
+// columns (chunks 0, 1).  Returns the sum of P.
+template <int ET>
 __device__ __forceinline__ float exp_keys_lo(uint32_t (&lo)[64], uint32_t (&hi)[64], uint32_t tS,
                                              uint64_t c2, uint64_t negm2, bool masked,
                                              int lim_blk) {
@@ -324,16 +359,16 @@ __device__ __forceinline__ float exp_keys_lo(uint32_t (&lo)[64], uint32_t (&hi)[
   tmem_ld_wait_x32(c1);
   tmem_ld_x32_async(tS + 64, c2r);
   if (masked) mask_keys<0, 64>(lo, lim_blk);
-  float sum = exp_chunk<BF16>(c0, c2, negm2, pk);
-  tmem_st_x16_async(tS, pk);
-  sum += exp_chunk<BF16>(c1, c2, negm2, pk);
-  tmem_st_x16_async(tS + 16, pk);
+  float sum = exp_chunk<ET>(c0, c2, negm2, pk);
+  store_p<ET>(tS, 0, pk);
+  sum += exp_chunk<ET>(c1, c2, negm2, pk);
+  store_p<ET>(tS, 1, pk);
   return sum;
 }
 
 // Keys 64-127 (the load of 64-95 issued by exp_keys_lo; 96-127 follows it);
-// P to TMEM columns [32,64).  Returns the sum of P.
-template <bool BF16>
+// P chunks 2, 3.  Returns the sum of P.
+template <int ET>
 __device__ __forceinline__ float exp_keys_hi(uint32_t (&hi)[64], uint32_t tS, uint64_t c2,
                                              uint64_t negm2, bool masked, int lim_blk) {
   uint32_t(&c2r)[32] = *reinterpret_cast<uint32_t(*)[32]>(&hi[0]);
@@ -342,33 +377,35 @@ __device__ __forceinline__ float exp_keys_hi(uint32_t (&hi)[64], uint32_t tS, ui
   tmem_ld_wait_x32(c2r);
   tmem_ld_x32_async(tS + 96, c3);
   if (masked) mask_keys<64, 32>(c2r, lim_blk);
-  float sum = exp_chunk<BF16>(c2r, c2, negm2, pk);
-  tmem_st_x16_async(tS + 32, pk);
+  float sum = exp_chunk<ET>(c2r, c2, negm2, pk);
+  store_p<ET>(tS, 2, pk);
   tmem_ld_wait_x32(c3);
   if (masked) mask_keys<96, 32>(c3, lim_blk);
-  sum += exp_chunk<BF16>(c3, c2, negm2, pk);
-  tmem_st_x16_async(tS + 48, pk);
+  sum += exp_chunk<ET>(c3, c2, negm2, pk);
+  store_p<ET>(tS, 3, pk);
   return sum;
 }
 
-// P of 64 keys already in registers, to TMEM at tP (32 columns, no wait).
-template <bool BF16>
-__device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, float m, uint32_t tP) {
+// P of key half `half` (64 keys already in registers) against m, to its P
+// columns from tP (no wait).  Returns the sum of P.
+template <int ET>
+__device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, float m, uint32_t tP,
+                                               int half) {
   const uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
   uint32_t pk[16];
-  float sum = exp_chunk<BF16>(s, c2, negm2, pk);
-  tmem_st_x16_async(tP, pk);
-  sum += exp_chunk<BF16>(s + 32, c2, negm2, pk);
-  tmem_st_x16_async(tP + 16, pk);
+  float sum = exp_chunk<ET>(s, c2, negm2, pk);
+  store_p<ET>(tP, 2 * half, pk);
+  sum += exp_chunk<ET>(s + 32, c2, negm2, pk);
+  store_p<ET>(tP, 2 * half + 1, pk);
   return sum;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, int ET, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, ET>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -482,10 +519,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
-          const CUtensorMap* m = kv ? &tm_v : &tm_k;
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m,
-                             &ctl.kv_full[slot], cb * 64, j * kBN, u.bh, pol_kv);
+          if (ET == kE4M3 && kv) {
+            // V transposed: one box of 128 keys x 128 rows (d)
+            tma_load_3d_warp(sRing + slot * C::kSlotBytes, &tm_v, &ctl.kv_full[slot], j * kBN, 0,
+                             u.bh, pol_kv);
+          } else {
+            const CUtensorMap* m = kv ? &tm_v : &tm_k;
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m,
+                               &ctl.kv_full[slot], cb * C::kBoxElems, j * kBN, u.bh, pol_kv);
+          }
           ++it;
           if (j == 0 && kv == 1) {
             // Q after K_0 and V_0: the previous unit's last Q K^T frees the
@@ -496,9 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx_warp(&ctl.q_full, 2 * C::kTileBytes);
             for (int t = 0; t < 2; ++t)
-              for (int cb = 0; cb < D / 64; ++cb)
+              for (int cb = 0; cb < C::kColBlocks; ++cb)
                 tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full,
-                                 cb * 64, q0 + t * kBM, u.bh, pol_q);
+                                 cb * C::kBoxElems, q0 + t * kBM, u.bh, pol_q);
             ++nq;
           }
           if (p.dynamic && j == nkv1 / 2 && kv == 1) {
@@ -512,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the next unit's Q into L2 while this unit still streams
               const Unit un = decode_unit<CAUSAL>(x_next, p);
               for (int t = 0; t < 2; ++t)
-                for (int cb = 0; cb < D / 64; ++cb)
-                  tma_prefetch_3d_warp(&tm_q, cb * 64, un.qb * 2 * kBM + t * kBM, un.bh);
+                for (int cb = 0; cb < C::kColBlocks; ++cb)
+                  tma_prefetch_3d_warp(&tm_q, cb * C::kBoxElems, un.qb * 2 * kBM + t * kBM, un.bh);
             }
           }
         }
@@ -542,7 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q1_lo = sdesc_lo(sQ + C::kTileBytes, kLboKMajor);
     auto slot_addr = [&](uint32_t item) { return sRing + (item % C::kStages) * C::kSlotBytes; };
     auto k_lo = [&](uint32_t item) { return sdesc_lo(slot_addr(item), kLboKMajor); };
-    auto v_lo = [&](uint32_t item) { return sdesc_lo(slot_addr(item), kLboV); };
+    auto v_lo = [&](uint32_t item) {
+      return sdesc_lo(slot_addr(item), ET == kE4M3 ? kLboKMajor : kLboV);
+    };
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       const bool good =
           mbar_wait(bar, parity, abort_flag, p.status, kStatusTimeoutMma, p.wait_limit_ns);
@@ -558,11 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto pv_halves = [&](int t, uint32_t tO, uint32_t tP, uint32_t vlo, uint32_t g, int j) {
       if (!wait(&ctl.p_half[t][0], g & 1)) return false;
       tc_fence_after();
-      issue_pv_half<D, BF16>(tO, tP, vlo, 0, j > 0);
+      issue_pv_half<D, ET>(tO, tP, vlo, 0, j > 0);
       mma_commit_warp(&ctl.pva_done[t]);
       if (!wait(&ctl.p_half[t][1], g & 1)) return false;
       tc_fence_after();
-      issue_pv_half<D, BF16>(tO, tP, vlo, 1, true);
+      issue_pv_half<D, ET>(tO, tP, vlo, 1, true);
       if constexpr (C::kSplitP) mma_commit_warp(&ctl.pvb_done[t]);
       return true;
     };
@@ -587,12 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = (g0 == 0 || wait(&ctl.s_free[0], (g0 - 1) & 1));
         if (!ok) break;
         tc_fence_after();
-        issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
+        issue_qk<D, ET>(tS0, q0_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[0]);
         ok = (g1 == 0 || wait(&ctl.s_free[1], (g1 - 1) & 1));
         if (!ok) break;
         tc_fence_after();
-        issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
+        issue_qk<D, ET>(tS1, q1_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[1]);
         mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
         if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
@@ -603,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_full(ik) && wait(&ctl.s_free[0], (g0 + j) & 1);
             if (!ok) break;
             tc_fence_after();
-            issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
+            issue_qk<D, ET>(tS0, q0_lo, k_lo(ik));
             mma_commit_warp(&ctl.s_full[0]);
           }
           ok = wait_full(iv);
@@ -615,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_full(ik) && wait(&ctl.s_free[1], (g1 + j) & 1);
             if (!ok) break;
             tc_fence_after();
-            issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+            issue_qk<D, ET>(tS1, q1_lo, k_lo(ik));
             mma_commit_warp(&ctl.s_full[1]);
             mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
             if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
@@ -627,9 +672,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         tc_fence_after();
-        issue_qk<D, BF16>(tS0, q0_lo, k_lo(it));
+        issue_qk<D, ET>(tS0, q0_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[0]);
-        issue_qk<D, BF16>(tS1, q1_lo, k_lo(it));
+        issue_qk<D, ET>(tS1, q1_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[1]);
         mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
         if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
@@ -648,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_full(ik);
             tc_fence_after();
             if (ok && j + 1 < nkv0) {
-              issue_qk<D, BF16>(tS0, q0_lo, k_lo(ik));
+              issue_qk<D, ET>(tS0, q0_lo, k_lo(ik));
               mma_commit_warp(&ctl.s_full[0]);
             }
           }
@@ -657,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
           if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
           if (more) {
-            issue_qk<D, BF16>(tS1, q1_lo, k_lo(ik));
+            issue_qk<D, ET>(tS1, q1_lo, k_lo(ik));
             mma_commit_warp(&ctl.s_full[1]);
             mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
             if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
@@ -681,6 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = lane_base + C::kOCol + t * D;
     const uint32_t tP = C::kSplitP ? lane_base + C::kPCol + t * 64 : tS;  // P_t
     const float cl2 = p.scale_log2;
+    // 0 at compile time for 16-bit P (x - 0.f folds to x exactly)
+    const float shift = ET == kE4M3 ? p.p_shift : 0.f;
     bool ok = true;
     uint32_t g = 0;  // key blocks done by this tile over all units of the block
     for (uint32_t k = 0; ok; ++k) {
@@ -748,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j == 0) m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
           if (gj > 0 && !wait_all(&ctl.pva_done[t], (gj - 1) & 1)) break;
-          float la = exp_keys_regs<BF16>(lo, cl2, m, tP);
+          float la = exp_keys_regs<ET>(lo, cl2, m - shift, tP, 0);
           // (the lazy-maximum test of the streaming path below, on registers)
           bool check = j > 0 && la > p.two_pow_tau;
           if (__any_sync(0xffffffffu, check)) {
@@ -762,14 +809,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (raise) m = bmax;
               l *= alpha;
               tmem_st_wait();
-              la = exp_keys_regs<BF16>(lo, cl2, m, tP);
+              la = exp_keys_regs<ET>(lo, cl2, m - shift, tP, 0);
               rescale_o(alpha);
             }
           }
           l += la;
           release(0);
           if (gj > 0 && !wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
-          float lb = exp_keys_regs<BF16>(hi, cl2, m, tP + 32);
+          float lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
           check = j > 0 && lb > p.two_pow_tau;
           if (__any_sync(0xffffffffu, check)) {
             const float bmax = row_max<64>(hi) * cl2;
@@ -782,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (raise) m = bmax;
               l *= alpha;
               tmem_st_wait();
-              lb = exp_keys_regs<BF16>(hi, cl2, m, tP + 32);
+              lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
               rescale_o(alpha);
             }
           }
@@ -796,9 +843,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mask_keys<64, 64>(hi, lim_blk);
           }
           m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
-          l = exp_keys_regs<BF16>(lo, cl2, m, tS);
+          l = exp_keys_regs<ET>(lo, cl2, m - shift, tS, 0);
           release(0);
-          l += exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+          l += exp_keys_regs<ET>(hi, cl2, m - shift, tS, 1);
           release(1);
         } else {
           // Exponentiate against the running maximum as S arrives from TMEM,
@@ -807,8 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tau and its P stands as computed; only a larger sum (rare once m has
           // settled: p <= 1 while the block maximum stays below m) needs the
           // exact maximum of that half.
-          uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-m, -m);
-          float la = exp_keys_lo<BF16>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
+          uint64_t c2 = f2_pack(cl2, cl2), negm2 = f2_pack(-(m - shift), -(m - shift));
+          float la = exp_keys_lo<ET>(lo, hi, tS, c2, negm2, masked_block, lim_blk);
           bool check = la > p.two_pow_tau;
           if (__any_sync(0xffffffffu, check)) {
             const float bmax = row_max<64>(lo) * cl2;
@@ -820,14 +867,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (raise) m = bmax;
               l *= alpha;
               tmem_st_wait();
-              la = exp_keys_regs<BF16>(lo, cl2, m, tS);
+              la = exp_keys_regs<ET>(lo, cl2, m - shift, tS, 0);
               rescale_o(alpha);
-              negm2 = f2_pack(-m, -m);
+              negm2 = f2_pack(-(m - shift), -(m - shift));
             }
           }
           l += la;
           release(0);
-          const float lb = exp_keys_hi<BF16>(hi, tS, c2, negm2, masked_block, lim_blk);
+          const float lb = exp_keys_hi<ET>(hi, tS, c2, negm2, masked_block, lim_blk);
           check = lb > p.two_pow_tau;
           float lhi = lb;
           if (__any_sync(0xffffffffu, check)) {
@@ -849,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (raise) m = bmax;
               l *= alpha;
               tmem_st_wait();
-              lhi = exp_keys_regs<BF16>(hi, cl2, m, tS + 32);
+              lhi = exp_keys_regs<ET>(hi, cl2, m - shift, tS, 1);
               rescale_o(alpha);
             }
           }
@@ -859,7 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       g += nkv;
 
-      // ---- epilogue: O / l in the storage dtype, LSE = ln 2 * (m + log2 l)
+      // ---- epilogue: O / l in the output dtype (the input's, bf16 for E4M3
+      // inputs), LSE = ln 2 * (m + log2 l - p_shift)
       if (ok) {
         ok = mbar_wait(&ctl.o_full[t], k & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
                        p.wait_limit_ns);
@@ -878,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pkd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pkd[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv_l,
+          pkd[i] = pack2<ET != kF16>(__uint_as_float(orr[2 * i]) * inv_l,
                                __uint_as_float(orr[2 * i + 1]) * inv_l);
         if (store) {
           uint4* dst = reinterpret_cast<uint4*>(orow + ch * 64);
@@ -892,7 +940,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.o_empty[t]);
       if (store)
-        p.lse[static_cast<size_t>(u.bh) * S + row] = (m + lg2(l)) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(u.bh) * S + row] =
+            (m + lg2(l) - shift) * 0.69314718055994530942f;
     }
   }
 
@@ -909,10 +958,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // linkage keeps the flags private to each loaded copy of the library (a
 // function-local static of an inline template would otherwise become one
 // process-wide symbol shared by every copy).
-template <int D, bool BF16, bool CAUSAL>
+template <int D, int ET, bool CAUSAL>
 static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& prm, unsigned grid, cudaStream_t stream) {
-  auto kern = fmha_fwd_kernel<D, BF16, CAUSAL>;
+  auto kern = fmha_fwd_kernel<D, ET, CAUSAL>;
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> opted_in[kMaxDevices];
   int dev = 0;
@@ -920,11 +969,11 @@ static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D>::kSmemBytes);
+                             Cfg<D, ET>::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  kern<<<grid, kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, prm);
   return cudaGetLastError();
 }
 

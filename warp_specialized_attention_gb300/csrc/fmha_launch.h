@@ -18,4 +18,9 @@ cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap& tq, const
                             const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
                             cudaStream_t stream);
 
+// E4M3 inputs, head dim 128: tvt maps V transposed, (S, D, B*H).
+cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tvt, const FwdParams& prm, unsigned grid,
+                            cudaStream_t stream);
+
 }  // namespace wsa

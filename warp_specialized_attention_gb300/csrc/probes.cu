@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(128, 1)
     bool loaded = mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs);
     if (__all_sync(0xffffffffu, loaded)) {
       tc_fence_after();
-      issue_qk<D, BF16>(tmem, sdesc_lo(sA, kLboKMajor), sdesc_lo(sB, kLboKMajor));
+      issue_qk<D, BF16 ? kBF16 : kF16>(tmem, sdesc_lo(sA, kLboKMajor), sdesc_lo(sB, kLboKMajor));
     }
     mma_commit_warp(&ctl.bar_mma);
   }
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(128, 1)
     bool loaded = mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs);
     if (__all_sync(0xffffffffu, loaded)) {
       tc_fence_after();
-      issue_pv<D, BF16>(tmem + 128, tmem, sdesc_lo(sV, kLboV), false);
+      issue_pv<D, BF16 ? kBF16 : kF16>(tmem + 128, tmem, sdesc_lo(sV, kLboV), false);
     }
     mma_commit_warp(&ctl.bar_mma);
   }
