@@ -51,7 +51,7 @@ import synthetic  # noqa: E402
 METRIC = "FMHA fwd TFLOPS at B4 H32 S16K D128 fp16; % of GB300 dense tensor peak"
 UNIT = "TFLOPS"
 KERNEL_SOURCES = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu",
-                  "fmha_api.cu"]
+                  "fmha_fwd_e4m3.cu", "fmha_api.cu"]
 
 
 # ----------------------------------------------------------------------------- helpers
