@@ -6,7 +6,8 @@ library (``warp_specialized_attention_gb300``) and neither imports the other;
 the only thing both sides consume is the seeded synthetic inputs.
 
 The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, two-pass
-softmax, OpenMP over independent rows).  This module compiles it with gcc into
+softmax, OpenMP over independent rows) and, for the backward pass (the
+gradients of that definition), in ``attn_oracle_bwd.c``.  This module compiles it with gcc into
 ``_attn_oracle.so`` beside the source and marshals numpy float64 arrays into it.
 The definition it follows -- attention split into Q K^T, softmax and P V as in
 "Tawa: Automatic Warp Specialization for Modern GPUs with Asynchronous
@@ -23,6 +24,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRC_BWD = os.path.join(_HERE, "attn_oracle_bwd.c")
 _LIB = os.path.join(_HERE, "_attn_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -31,11 +33,11 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the C oracle into ``_attn_oracle.so`` (gcc, -O2, OpenMP)."""
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB) >= max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_BWD))):
         return _LIB
     tmp = _LIB + ".tmp.%d" % os.getpid()
     cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
-           "-o", tmp, _SRC, "-lm"]
+           "-o", tmp, _SRC, _SRC_BWD, "-lm"]
     subprocess.run(cmd, check=True, capture_output=True, text=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -57,6 +59,10 @@ def _load():
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_double,
                                              dp, dp]
             lib.attn_oracle_full.restype = ctypes.c_int
+            lib.attn_oracle_bwd_slice.argtypes = [dp, dp, dp, dp, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int,
+                                                  ctypes.c_double, dp, dp, dp]
+            lib.attn_oracle_bwd_slice.restype = ctypes.c_int
             lib.attn_oracle_threads.argtypes = []
             lib.attn_oracle_threads.restype = ctypes.c_int
             _lib = lib
@@ -114,3 +120,26 @@ def attention(q, k, v, causal: bool, scale: float):
     if rc != 0:
         raise RuntimeError("attn_oracle_full failed with code %d" % rc)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal: bool, scale: float):
+    """Gradients of the forward definition with respect to q, k, v, given dO.
+
+    q, k, v, dout: (..., S, D).  Returns (dq, dk, dv) as float64."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if not (q.shape == k.shape == v.shape == dout.shape) or q.ndim < 2:
+        raise ValueError("q, k, v, dout must share one (..., S, D) shape")
+    S, D = q.shape[-2:]
+    flat = [t.reshape(-1, S, D) for t in (q, k, v, dout)]
+    outs = [np.empty((flat[0].shape[0], S, D), dtype=np.float64) for _ in range(3)]
+    lib = _load()
+    for bh in range(flat[0].shape[0]):
+        sl = [np.ascontiguousarray(t[bh]) for t in flat]
+        res = [np.empty((S, D), dtype=np.float64) for _ in range(3)]
+        rc = lib.attn_oracle_bwd_slice(*(_ptr(t) for t in sl), S, D, int(bool(causal)),
+                                       float(scale), *(_ptr(r) for r in res))
+        if rc != 0:
+            raise RuntimeError("attn_oracle_bwd_slice failed with code %d" % rc)
+        for o, r in zip(outs, res):
+            o[bh] = r
+    return tuple(o.reshape(q.shape) for o in outs)
