@@ -36,6 +36,15 @@ int wsa_probe_pv(const void* p, const void* v, float* o, int D, int bf16);
 int wsa_probe_qk_e4m3(const void* a, const void* b, float* c);
 int wsa_probe_pv_e4m3(const void* p, const void* vt, float* o);
 
+/* The two shared-memory forms of the backward pass, one 128 x 128 x D tile
+ * (16-bit, D = 64 or 128; bf16 when bf16 != 0), c fp32 row-major [128][D]:
+ *   wsa_probe_kmaj_mn: c = a b,  a[128][128] row-major (read K-major),
+ *                                b[128][D] row-major (read MN-major)
+ *   wsa_probe_mn_mn:   c = at^T b, at[128][128] row-major holding A
+ *                                transposed (read MN-major), b as above */
+int wsa_probe_kmaj_mn(const void* a, const void* b, float* c, int D, int bf16);
+int wsa_probe_mn_mn(const void* at, const void* b, float* c, int D, int bf16);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,9 @@ def probes():
     for f in (lib.wsa_probe_qk_e4m3, lib.wsa_probe_pv_e4m3):
         f.argtypes = [ctypes.c_void_p] * 3
         f.restype = ctypes.c_int
+    for f in (lib.wsa_probe_kmaj_mn, lib.wsa_probe_mn_mn):
+        f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int]
+        f.restype = ctypes.c_int
     return lib
 
 
@@ -87,4 +90,37 @@ def test_pv_tile_e4m3(probes):
     pd, vtd = p8.cuda(), v8.T.contiguous().cuda()   # V goes in transposed: vt[d][key]
     assert probes.wsa_probe_pv_e4m3(pd.data_ptr(), vtd.data_ptr(), o.data_ptr()) == 0
     err = (o.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_kmaj_mn_tile(probes, D, dtype):
+    """The backward's dK form: A K-major (dS^T), B MN-major (Q)."""
+    g = torch.Generator().manual_seed(31 + D)
+    a = torch.randn(128, 128, generator=g).to(dtype)
+    b = torch.randn(128, D, generator=g).to(dtype)
+    ref = a.double() @ b.double()
+    c = torch.full((128, D), float("nan"), device="cuda")
+    ad, bd = a.cuda(), b.cuda()
+    assert probes.wsa_probe_kmaj_mn(ad.data_ptr(), bd.data_ptr(), c.data_ptr(), D,
+                                    int(dtype == torch.bfloat16)) == 0
+    err = (c.cpu().double() - ref).abs().max().item()
+    assert err < 1e-3, "max abs error %g" % err
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_mn_mn_tile(probes, D, dtype):
+    """The backward's dQ form: A read MN-major from its transpose (the dS^T
+    tile read as dS), B MN-major (K)."""
+    g = torch.Generator().manual_seed(37 + D)
+    a = torch.randn(128, 128, generator=g).to(dtype)
+    b = torch.randn(128, D, generator=g).to(dtype)
+    ref = a.double() @ b.double()
+    c = torch.full((128, D), float("nan"), device="cuda")
+    atd, bd = a.T.contiguous().cuda(), b.cuda()
+    assert probes.wsa_probe_mn_mn(atd.data_ptr(), bd.data_ptr(), c.data_ptr(), D,
+                                  int(dtype == torch.bfloat16)) == 0
+    err = (c.cpu().double() - ref).abs().max().item()
     assert err < 1e-3, "max abs error %g" % err

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "fmha_bwd_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
 #include "wsattn_probes.h"
 
@@ -280,6 +281,72 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// The backward pass's two SS forms on one tile: C[128][D] (fp32) = A B with
+// x = the 128 x 128 16-bit tile holding A (MODE 0: A itself, K-major; MODE 1:
+// A transposed, read MN-major) and y = B[128][D] (rows = K, read MN-major).
+template <int D, bool BF16, int MODE>
+__global__ void __launch_bounds__(128, 1)
+    probe_bwd_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty,
+                     float* c) {
+  extern __shared__ uint8_t raw[];
+  const uint32_t raw_addr = smem_u32(raw);
+  uint8_t* sm = raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sX = smem_u32(sm), sY = sX + 128 * 128 * 2;
+  ProbeSmem& ctl = *reinterpret_cast<ProbeSmem*>(sm + 128 * 128 * 2 + 128 * D * 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.bar_load, 1);
+    mbar_init(&ctl.bar_mma, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl.tmem_base, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* ab = &ctl.abort;
+  constexpr int kET = BF16 ? kBF16 : kF16;
+  if (warp == 0) {
+    mbar_arrive_expect_tx_warp(&ctl.bar_load, 128 * 128 * 2 + 128 * D * 2);
+    for (int cb = 0; cb < 2; ++cb)
+      tma_load_3d_warp(sX + cb * 128 * 128, &tx, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
+    for (int cb = 0; cb < D / 64; ++cb)
+      tma_load_3d_warp(sY + cb * 128 * 128, &ty, &ctl.bar_load, cb * 64, 0, 0, policy_evict_first());
+    bool loaded = mbar_wait(&ctl.bar_load, 0, ab, &g_probe_status, 1, kProbeWaitNs);
+    if (__all_sync(0xffffffffu, loaded)) {
+      tc_fence_after();
+      if (MODE == 0)
+        issue_kmaj_mn<D, kET>(tmem, sdesc_lo(sX, kLboKMajor), sdesc_lo(sY, kLboV), false);
+      else
+        issue_mn_mn<D, kET>(tmem, sdesc_lo(sX, kLboV), sdesc_lo(sY, kLboV), false);
+    }
+    mma_commit_warp(&ctl.bar_mma);
+  }
+  __syncwarp();
+  bool ok = mbar_wait(&ctl.bar_mma, 0, nullptr, &g_probe_status, 2, kProbeWaitNs);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) {
+    tc_fence_after();
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int row = warp * 32 + lane;
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t r[32];
+      tmem_ld_x32(lane_base + ch * 32, r);
+      for (int j = 0; j < 32; ++j) c[row * D + ch * 32 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -362,6 +429,26 @@ int probe_status() {
   return 0;
 }
 
+template <int D, bool BF16, int MODE>
+int run_bwd(const void* x, const void* y, float* c) {
+  CUtensorMap tx, ty;
+  if (!encode_tile(&tx, x, 128, BF16) || !encode_tile(&ty, y, D, BF16)) return 3;
+  const int smem = 1024 + 128 * 128 * 2 + 128 * D * 2 + 256;
+  auto k = probe_bwd_kernel<D, BF16, MODE>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 3;
+  k<<<1, 128, smem>>>(tx, ty, c);
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
+}
+
+template <int MODE>
+int dispatch_bwd(const void* x, const void* y, float* c, int D, int bf16) {
+  if (D == 64) return bf16 ? run_bwd<64, true, MODE>(x, y, c) : run_bwd<64, false, MODE>(x, y, c);
+  if (D == 128)
+    return bf16 ? run_bwd<128, true, MODE>(x, y, c) : run_bwd<128, false, MODE>(x, y, c);
+  return 2;
+}
+
 int run_qk_e4m3(const void* a, const void* b, float* c) {
   CUtensorMap ta, tb;
   if (!encode_tile_u8(&ta, a) || !encode_tile_u8(&tb, b)) return 3;
@@ -425,6 +512,20 @@ int wsa_probe_pv_e4m3(const void* p, const void* vt, float* o) {
   if (!p || !vt || !o || (reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(vt)) & 15)
     return 1;
   const int r = run_pv_e4m3(p, vt, o);
+  return r ? r : probe_status();
+}
+
+int wsa_probe_kmaj_mn(const void* a, const void* b, float* c, int D, int bf16) {
+  if (!a || !b || !c || (reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15)
+    return 1;
+  const int r = dispatch_bwd<0>(a, b, c, D, bf16);
+  return r ? r : probe_status();
+}
+
+int wsa_probe_mn_mn(const void* at, const void* b, float* c, int D, int bf16) {
+  if (!at || !b || !c || (reinterpret_cast<uintptr_t>(at) | reinterpret_cast<uintptr_t>(b)) & 15)
+    return 1;
+  const int r = dispatch_bwd<1>(at, b, c, D, bf16);
   return r ? r : probe_status();
 }
 

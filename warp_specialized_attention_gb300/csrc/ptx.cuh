@@ -152,6 +152,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with the major-ness of both operands chosen (bit 15: A, bit 16: B;
+// 1 = MN-major, i.e. the M or N index contiguous in shared memory).
+__host__ __device__ constexpr uint32_t idesc_f16_ab(bool bf16, int M, int N, bool a_mn_major,
+                                                    bool b_mn_major) {
+  return idesc_f16(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 descriptor version (1),
