@@ -34,6 +34,7 @@
 #ifndef WSATTN_H_
 #define WSATTN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -122,6 +123,47 @@ fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, 
                           void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
                           int64_t H, int64_t S, int64_t D, int causal, float scale,
                           fmha_dtype dtype, int n_chunks, void* stream);
+
+/*
+ * fmha_bwd_workspace_bytes -- bytes of device scratch fmha_bwd needs:
+ * B*H*S*D + B*H*S fp32 values (a dQ accumulator and the per-row delta).
+ * 0 for non-positive sizes.
+ */
+size_t fmha_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * fmha_bwd -- backward pass of fmha_fwd: the gradients dQ, dK, dV of a loss L
+ * given dO = dL/dO.  The pages schedule this kernel as well ("Optimal Software
+ * Pipelining and Warp Specialization for Tensor Core GPUs", Sections 6.3-6.4,
+ * FlashAttention backward) without writing it out; it is the chain rule of the
+ * definition above, per (batch, head):
+ *
+ *     P = softmax(scale Q K^T [+ mask]) = exp(scale Q K^T - LSE)   (row-wise)
+ *     dV = P^T dO,   dP = dO V^T,   delta_i = dO_i . O_i,
+ *     dS = P * (dP - delta),   dQ = scale dS K,   dK = scale dS^T Q.
+ *
+ *   q, k, v, o, lse   the forward's inputs, output and LSE (layouts as in
+ *                     fmha_fwd; lse must come from the same q, k, v, scale,
+ *                     causal).  Read only.
+ *   d_o               device, (B, H, S, D) `dtype`.  Read only.
+ *   dq, dk, dv        device, (B, H, S, D) `dtype`.  Written.
+ *   workspace         device scratch of at least fmha_bwd_workspace_bytes()
+ *                     bytes, 16-byte aligned, owned by the caller; its contents
+ *                     on entry do not matter and are undefined on return.
+ *   dtype             FMHA_F16 or FMHA_BF16 (FMHA_E4M3 -> FMHA_ERR_UNSUPPORTED);
+ *                     D 64 or 128; other arguments as fmha_fwd.
+ *
+ * All device pointers 16-byte aligned (lse 4); outputs and workspace must not
+ * overlap each other or any input.  Asynchronous on `stream`: a memset and
+ * three kernels are enqueued (delta, the warp-specialized backward, the dQ
+ * conversion); no memory is allocated.  dQ is accumulated with fp32 atomic
+ * additions across key blocks, so its last bits may differ between runs.
+ * Errors as fmha_fwd.
+ */
+fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* d_o, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int64_t B, int64_t H, int64_t S, int64_t D,
+                     int causal, float scale, fmha_dtype dtype, void* stream);
 
 /*
  * fmha_get_device_status -- synchronise `stream`, then report and clear the

@@ -25,6 +25,7 @@ __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
     "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
+    "fmha_bwd", "fmha_bwd_workspace_bytes", "attention_backward",
     "get_device_status", "status_str", "version",
 ]
 
@@ -75,6 +76,11 @@ def load_library():
         lib.fmha_fwd_host.restype = ctypes.c_int
         lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double, ctypes.c_float]
         lib.fmha_fwd_testing.restype = ctypes.c_int
+        lib.fmha_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.fmha_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fmha_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t, i64, i64, i64, i64, ctypes.c_int,
+                                             ctypes.c_float, ctypes.c_int, vp]
+        lib.fmha_bwd.restype = ctypes.c_int
         lib.fmha_get_device_status.argtypes = [vp]
         lib.fmha_get_device_status.restype = ctypes.c_int
         lib.fmha_status_str.argtypes = [ctypes.c_int]
@@ -220,3 +226,49 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     fmha_fwd(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
     return o, lse
+
+
+def fmha_bwd_workspace_bytes(B: int, H: int, S: int, D: int) -> int:
+    """Bytes of device scratch fmha_bwd needs (C ABI fmha_bwd_workspace_bytes)."""
+    return int(load_library().fmha_bwd_workspace_bytes(B, H, S, D))
+
+
+def fmha_bwd(q, k, v, o, lse, d_o, dq, dk, dv, workspace=None, causal: bool = False,
+             scale: float | None = None, stream=None) -> None:
+    """Enqueue the backward pass (C ABI fmha_bwd): dq, dk, dv <- gradients of
+    attention(q, k, v) for the output gradient d_o, using the forward's o and
+    lse.  All (B, H, S, D) 16-bit CUDA tensors of one dtype, lse float32
+    (B, H, S).  ``workspace`` is a CUDA uint8 tensor of at least
+    fmha_bwd_workspace_bytes(B, H, S, D) bytes; one is allocated with torch
+    when it is None."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    for name, t in (("d_o", d_o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("%s must match q's shape and dtype" % name)
+    B, H, S, D = q.shape
+    need = fmha_bwd_workspace_bytes(B, H, S, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError("workspace must be a CUDA tensor of at least %d bytes" % need)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        st = lib.fmha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          d_o.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          B, H, S, D, int(bool(causal)), float(scale), _dtype_code(q),
+                          _stream_handle(stream))
+    if st != FMHA_OK:
+        raise FmhaError(st, "fmha_bwd", lib.fmha_last_cuda_error().decode())
+
+
+def attention_backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None,
+                       stream=None):
+    """Allocate dq, dk, dv (and the workspace) with torch and run fmha_bwd."""
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fmha_bwd(q, k, v, o, lse, d_o, dq, dk, dv, causal=causal, scale=scale, stream=stream)
+    return dq, dk, dv

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "fmha_bwd_sm103.cuh"
 #include "fmha_fwd_sm103.cuh"
 #include "fmha_launch.h"
 #include "wsattn.h"
@@ -193,6 +194,84 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   return FMHA_OK;
 }
 
+// ---------------------------------------------------------------- backward pass
+
+size_t bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S);
+  return rows * static_cast<size_t>(D) * 4 + rows * 4;  // dQ accumulator + delta, fp32
+}
+
+fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t S,
+                     int64_t D, int causal, float scale, int dtype, void* stream,
+                     uint64_t wait_limit_ns) {
+  if (dtype == FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
+  // q, k, v, o, lse as in the forward (o is an input here)
+  const fmha_status vs = validate(q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, H,
+                                  S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
+  if (!d_o || !dq || !dk || !dv || !workspace) return FMHA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(d_o) | reinterpret_cast<uintptr_t>(dq) |
+       reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+       reinterpret_cast<uintptr_t>(workspace)) & 15u)
+    return FMHA_ERR_INVALID_ARG;
+  const int64_t BH = B * H, n_blk = (S + 127) / 128;
+  if (n_blk * BH > (int64_t{1} << 31) - 1) return FMHA_ERR_INVALID_ARG;
+  const size_t need = bwd_workspace_bytes(B, H, S, D);
+  if (workspace_bytes < need) return FMHA_ERR_INVALID_ARG;
+  const size_t tb = static_cast<size_t>(BH * S * D) * 2, lb = static_cast<size_t>(BH * S) * 4;
+  const void* ins[6] = {q, k, v, o, d_o, lse};
+  const size_t in_sz[6] = {tb, tb, tb, tb, tb, lb};
+  void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_sz[4] = {tb, tb, tb, need};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j])) return FMHA_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j])) return FMHA_ERR_INVALID_ARG;
+  }
+
+  cudaError_t e;
+  EncodeTiledFn enc = encode_fn(&e);
+  if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
+  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  if (!encode_map(enc, &tq, q, dtype, BH, S, D) || !encode_map(enc, &tk, k, dtype, BH, S, D) ||
+      !encode_map(enc, &tv, v, dtype, BH, S, D) || !encode_map(enc, &tdo, d_o, dtype, BH, S, D))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  int* status = nullptr;
+  if ((e = status_word(&status)) != cudaSuccess)
+    return cuda_fail(e, "cudaGetSymbolAddress(status)");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == FMHA_BF16;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = dq_acc + static_cast<size_t>(BH * S * D);
+  if ((e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(BH * S * D) * 4, st)) != cudaSuccess)
+    return cuda_fail(e, "clear the dQ accumulator");
+  if ((e = wsa::launch_bwd_delta(static_cast<int>(D), bf16, o, d_o, delta, BH * S, st)) !=
+      cudaSuccess)
+    return cuda_fail(e, "delta kernel launch");
+  wsa::BwdParams prm;
+  prm.lse = lse;
+  prm.delta = delta;
+  prm.dq_accum = dq_acc;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.status = status;
+  prm.S = static_cast<int>(S);
+  prm.n_blk = static_cast<int>(n_blk);
+  prm.scale = scale;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.wait_limit_ns = wait_limit_ns;
+  if ((e = wsa::launch_bwd(static_cast<int>(D), bf16, causal != 0, tq, tk, tv, tdo, prm,
+                           static_cast<unsigned>(n_blk * BH), st)) != cudaSuccess)
+    return cuda_fail(e, "backward kernel launch");
+  if ((e = wsa::launch_bwd_dq(bf16, dq_acc, dq, BH * S * D, st)) != cudaSuccess)
+    return cuda_fail(e, "dQ conversion launch");
+  return FMHA_OK;
+}
+
 // Per host thread and device: the two copy streams and the events that chain
 // chunks between them and the caller's stream (created on first use).
 constexpr int kMaxChunks = 64;
@@ -323,6 +402,19 @@ fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, 
                           fmha_dtype dtype, int n_chunks, void* stream) {
   return fwd_host_impl(q, k, v, o, lse, dq, dk, dv, d_o, dlse, B, H, S, D, causal, scale,
                        static_cast<int>(dtype), n_chunks, stream);
+}
+
+size_t fmha_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
+  if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
+  return bwd_workspace_bytes(B, H, S, D);
+}
+
+fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* d_o, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, int64_t B, int64_t H, int64_t S, int64_t D,
+                     int causal, float scale, fmha_dtype dtype, void* stream) {
+  return bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, workspace, workspace_bytes, B, H, S, D,
+                  causal, scale, static_cast<int>(dtype), stream, kDefaultWaitLimitNs);
 }
 
 fmha_status fmha_get_device_status(void* stream) {

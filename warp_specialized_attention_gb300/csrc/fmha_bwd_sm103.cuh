@@ -46,4 +46,402 @@ __device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_lo, uint
   }
 }
 
+// ============================================================================ the kernel
+//
+// Attention backward for one (head, 128-key block) per block of 320 threads:
+//   warps 0-3  dS / P: key row 32w + lane; read S^T and dP^T from TMEM, write
+//              P^T (16-bit) over S^T in TMEM and dS^T to shared memory; at the
+//              end write dK and dV
+//   warps 4-7  dQ: query row 32(w-4) + lane; read each block's dQ part from
+//              TMEM and add it, scaled, into the fp32 accumulator in global
+//              memory (vector red.add: several key blocks add into one row)
+//   warp 8     TMEM allocation and the tcgen05.mma issuer
+//   warp 9     TMA producer: K, V once; Q, dO per query block; LSE and delta
+// Per query block the issuer runs S^T = K Q^T, dP^T = V dO^T, then (once P^T
+// and dS^T are in place) dV += P^T dO, dK += dS^T Q and dQ = dS K.  The
+// chain-rule arithmetic is that of the backward oracle:
+//   P = exp(scale q.k - LSE), dS = P (dP - delta), delta_i = dO_i . O_i,
+//   dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K.
+// Synchronisation is the same empty/full mbarrier scheme as the forward (Tawa,
+// Section III-B/III-E); every wait is bounded and raises the abort flag.
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kTile = 128 * D * 2;                // 128 rows x D, 16-bit
+  static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 3 * kTile;
+  static constexpr int kOffDS = 4 * kTile;                 // dS^T, 128 x 128 16-bit
+  static constexpr int kOffStat = kOffDS + 128 * 128 * 2;  // 2 x (LSE*log2e[128], delta[128])
+  static constexpr int kOffCtl = kOffStat + 2 * 256 * 4;
+  static constexpr int kSmemBytes = 1024 + kOffCtl + 256;
+  // TMEM columns: S^T (P^T over its first 64), dP^T (dQ reuses it), dV, dK
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128;
+  static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
+};
+
+struct BwdCtl {
+  uint64_t kv_full;
+  uint64_t q_full, q_free, do_full, do_free;
+  uint64_t stat_full[2], stat_free[2];
+  uint64_t sd_full;   // S^T and dP^T are in TMEM
+  uint64_t p_ready;   // P^T in TMEM and dS^T in shared memory
+  uint64_t ds_free;   // the dS^T tile has been read (dK and dQ done)
+  uint64_t dq_full, dq_free;
+  uint64_t acc_done;  // every MMA of the block is complete
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BwdCtl) <= 256, "control block size");
+
+struct BwdParams {
+  const float* lse;    // (B,H,S) natural log-sum-exp of the forward
+  const float* delta;  // (B,H,S) dO . O per row
+  float* dq_accum;     // (B,H,S,D) fp32, zero before the launch
+  void* dk;            // (B,H,S,D) 16-bit
+  void* dv;
+  int* status;
+  int S;
+  int n_blk;           // ceil(S / 128)
+  float scale;
+  float scale_log2;    // scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// tcgen05.ld 32 lanes x 32 bits, 16 columns, no wait.
+__device__ __forceinline__ void tmem_ld_x16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// tcgen05.wait::ld tied to the 16 destination registers of an async load.
+__device__ __forceinline__ void tmem_ld_wait_x16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+template <int D, int ET, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fmha_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  static_assert(ET != kE4M3, "backward: 16-bit inputs");
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+  BwdCtl& ctl = *reinterpret_cast<BwdCtl*>(smem + C::kOffCtl);
+  float* stats = reinterpret_cast<float*>(smem + C::kOffStat);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = p.S;
+  const int bh = blockIdx.x / p.n_blk;
+  const int kb = blockIdx.x - bh * p.n_blk;
+  const int qb0 = CAUSAL ? kb : 0;       // query blocks that see this key block
+  const int nq = p.n_blk - qb0;          // >= 1
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.kv_full, 1);
+    mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.q_free, 1);
+    mbar_init(&ctl.do_full, 1);
+    mbar_init(&ctl.do_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.stat_full[i], 1);
+      mbar_init(&ctl.stat_free[i], 4);
+    }
+    mbar_init(&ctl.sd_full, 1);
+    mbar_init(&ctl.p_ready, 4);
+    mbar_init(&ctl.ds_free, 1);
+    mbar_init(&ctl.dq_full, 1);
+    mbar_init(&ctl.dq_free, 4);
+    mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.mma_drain, 1);
+    ctl.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&ctl.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  volatile int* abort_flag = &ctl.abort;
+  const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sQ = sbase + C::kOffQ;
+  const uint32_t sDO = sbase + C::kOffDO, sDS = sbase + C::kOffDS;
+  auto wait = [&](uint64_t* bar, uint32_t parity, int code) {
+    bool good = mbar_wait(bar, parity, abort_flag, p.status, code, p.wait_limit_ns);
+    return __all_sync(0xffffffffu, good);
+  };
+
+  if (warp == kWarpLoad) {
+    // ================================================================ TMA producer
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+    const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
+    mbar_arrive_expect_tx_warp(&ctl.kv_full, 2 * C::kTile);
+    for (int cb = 0; cb < D / 64; ++cb) {
+      tma_load_3d_warp(sK + cb * (128 * 128), &tm_k, &ctl.kv_full, cb * 64, kb * 128, bh, pol_kv);
+      tma_load_3d_warp(sV + cb * (128 * 128), &tm_v, &ctl.kv_full, cb * 64, kb * 128, bh, pol_kv);
+    }
+    int nq_loads = 0, ndo_loads = 0;  // Q and dO tiles issued
+    for (int n = 0; n < nq; ++n) {
+      const int qb = qb0 + n;
+      if (n >= 1 && !wait(&ctl.q_free, (n - 1) & 1, kStatusTimeoutLoad)) break;
+      mbar_arrive_expect_tx_warp(&ctl.q_full, C::kTile);
+      for (int cb = 0; cb < D / 64; ++cb)
+        tma_load_3d_warp(sQ + cb * (128 * 128), &tm_q, &ctl.q_full, cb * 64, qb * 128, bh, pol_q);
+      ++nq_loads;
+      if (n >= 1 && !wait(&ctl.do_free, (n - 1) & 1, kStatusTimeoutLoad)) break;
+      mbar_arrive_expect_tx_warp(&ctl.do_full, C::kTile);
+      for (int cb = 0; cb < D / 64; ++cb)
+        tma_load_3d_warp(sDO + cb * (128 * 128), &tm_do, &ctl.do_full, cb * 64, qb * 128, bh,
+                         pol_q);
+      ++ndo_loads;
+      // this block's LSE (in log2 units) and delta; rows past S: P = 0
+      const int buf = n & 1;
+      if (n >= 2 && !wait(&ctl.stat_free[buf], ((n >> 1) - 1) & 1, kStatusTimeoutLoad)) break;
+      float* st = stats + buf * 256;
+      for (int r = lane; r < 128; r += 32) {
+        const int q = qb * 128 + r;
+        const size_t idx = static_cast<size_t>(bh) * S + q;
+        st[r] = q < S ? p.lse[idx] * kLog2e : INFINITY;
+        st[128 + r] = q < S ? p.delta[idx] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.stat_full[buf]);
+    }
+    // Drain: every issued copy lands before the block may exit.
+    mbar_wait(&ctl.kv_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    if (nq_loads > 0)
+      mbar_wait(&ctl.q_full, (nq_loads - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
+                p.wait_limit_ns);
+    if (ndo_loads > 0)
+      mbar_wait(&ctl.do_full, (ndo_loads - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
+                p.wait_limit_ns);
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    const uint32_t k_lo = sdesc_lo(sK, kLboKMajor), v_lo = sdesc_lo(sV, kLboKMajor);
+    const uint32_t q_lo = sdesc_lo(sQ, kLboKMajor), do_lo = sdesc_lo(sDO, kLboKMajor);
+    const uint32_t k_mn = sdesc_lo(sK, kLboV), q_mn = sdesc_lo(sQ, kLboV);
+    const uint32_t do_mn = sdesc_lo(sDO, kLboV);
+    const uint32_t ds_k = sdesc_lo(sDS, kLboKMajor), ds_mn = sdesc_lo(sDS, kLboV);
+    bool ok = wait(&ctl.kv_full, 0, kStatusTimeoutMma);
+    for (int n = 0; ok && n < nq; ++n) {
+      ok = wait(&ctl.q_full, n & 1, kStatusTimeoutMma) &&
+           wait(&ctl.do_full, n & 1, kStatusTimeoutMma);
+      if (!ok) break;
+      tc_fence_after();
+      issue_qk<D, ET>(tmem + C::kColS, k_lo, q_lo);  // S^T = K Q^T
+      // dP^T takes the columns of the previous block's dQ part
+      if (n >= 1 && !(ok = wait(&ctl.dq_free, (n - 1) & 1, kStatusTimeoutMma))) break;
+      tc_fence_after();
+      issue_qk<D, ET>(tmem + C::kColDP, v_lo, do_lo);  // dP^T = V dO^T
+      mma_commit_warp(&ctl.sd_full);
+      if (!(ok = wait(&ctl.p_ready, n & 1, kStatusTimeoutMma))) break;
+      tc_fence_after();
+      issue_pv<D, ET>(tmem + C::kColDV, tmem + C::kColS, do_mn, n > 0);  // dV += P^T dO
+      issue_kmaj_mn<D, ET>(tmem + C::kColDK, ds_k, q_mn, n > 0);        // dK += dS^T Q
+      mma_commit_warp(&ctl.q_free);
+      mma_commit_warp(&ctl.do_free);
+      issue_mn_mn<D, ET>(tmem + C::kColDQ, ds_mn, k_mn, false);         // dQ part = dS K
+      mma_commit_warp(&ctl.dq_full);
+      mma_commit_warp(&ctl.ds_free);
+    }
+    mma_commit_warp(&ctl.acc_done);
+    mma_commit_warp(&ctl.mma_drain);
+    mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ================================================================ P and dS (key rows)
+    const int r = warp * 32 + lane;  // key row in the block, TMEM lane
+    const int key = kb * 128 + r;
+    const bool key_ok = key < S;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float cl2 = p.scale_log2;
+    bool ok = true;
+    for (int n = 0; ok && n < nq; ++n) {
+      const int qb = qb0 + n;
+      const int buf = n & 1;
+      ok = wait(&ctl.stat_full[buf], (n >> 1) & 1, kStatusTimeoutSoftmax) &&
+           wait(&ctl.sd_full, n & 1, kStatusTimeoutSoftmax) &&
+           (n == 0 || wait(&ctl.ds_free, (n - 1) & 1, kStatusTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      const float* lse2 = stats + buf * 256;
+      const float* dl = lse2 + 128;
+      const bool diag = CAUSAL && qb == kb;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {  // 16 queries per chunk
+        uint32_t sv[16], dpv[16];
+        tmem_ld_x16_async(lane_base + C::kColS + c * 16, sv);
+        tmem_ld_x16_async(lane_base + C::kColDP + c * 16, dpv);
+        tmem_ld_wait_x16(sv);
+        tmem_ld_wait_x16(dpv);
+        uint32_t pk[16], dk16[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int qi = c * 16 + e + h;
+            const bool vis = key_ok && !(diag && r > qi);
+            const float pv = vis ? ex2(__uint_as_float(sv[e + h]) * cl2 - lse2[qi]) : 0.f;
+            pp[h] = pv;
+            dd[h] = pv * (__uint_as_float(dpv[e + h]) - dl[qi]);
+          }
+          pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
+          dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
+        }
+        tmem_st_x8_async(lane_base + C::kColS + c * 8, pk);  // P^T over S^T
+        // dS^T row r, queries 16c..16c+15: two 16-byte units of the
+        // 128-byte-swizzled tile (unit index XOR row % 8)
+        const uint32_t cb = c >> 2, u0 = (c & 3) * 2;
+        const uint32_t row_addr = sDS + cb * (128 * 128) + r * 128;
+        const uint32_t a0 = row_addr + ((u0 ^ (r & 7)) << 4);
+        const uint32_t a1 = row_addr + (((u0 + 1) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(dk16[0]),
+                     "r"(dk16[1]), "r"(dk16[2]), "r"(dk16[3])
+                     : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(dk16[4]),
+                     "r"(dk16[5]), "r"(dk16[6]), "r"(dk16[7])
+                     : "memory");
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // dS^T stores -> visible to the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl.p_ready);
+        mbar_arrive(&ctl.stat_free[buf]);
+      }
+    }
+    // ---- epilogue: dV and dK (x scale) in the storage dtype
+    if (ok) {
+      ok = wait(&ctl.acc_done, 0, kStatusTimeoutSoftmax);
+    }
+    if (ok) {
+      tc_fence_after();
+      const size_t row_off = (static_cast<size_t>(bh) * S + (key_ok ? key : 0)) * D * 2;
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        uint8_t* out = reinterpret_cast<uint8_t*>(t ? p.dk : p.dv) + row_off;
+        const float mul = t ? p.scale : 1.f;
+        const uint32_t col = t ? C::kColDK : C::kColDV;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t orr[32];
+          tmem_ld_x32(lane_base + col + ch * 32, orr);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = pack2<ET == kBF16>(__uint_as_float(orr[2 * i]) * mul,
+                                        __uint_as_float(orr[2 * i + 1]) * mul);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ================================================================ dQ (query rows)
+    const int quad = warp & 3;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    bool ok = true;
+    for (int n = 0; ok && n < nq; ++n) {
+      const int q = (qb0 + n) * 128 + quad * 32 + lane;
+      if (!(ok = wait(&ctl.dq_full, n & 1, kStatusTimeoutSoftmax))) break;
+      tc_fence_after();
+      float* dst = p.dq_accum + (static_cast<size_t>(bh) * S + (q < S ? q : 0)) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_x32(lane_base + C::kColDQ + ch * 32, r);
+        if (q < S) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            red_add_v4(dst + ch * 32 + 4 * i, __uint_as_float(r[4 * i]) * p.scale,
+                       __uint_as_float(r[4 * i + 1]) * p.scale,
+                       __uint_as_float(r[4 * i + 2]) * p.scale,
+                       __uint_as_float(r[4 * i + 3]) * p.scale);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dq_free);
+    }
+  }
+
+  // ---- teardown: every role has drained its asynchronous work
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// delta_i = dO_i . O_i in fp32, one warp per row.
+template <int D, int ET>
+__global__ void __launch_bounds__(256) fmha_bwd_delta_kernel(const void* o, const void* d_o,
+                                                             float* delta, int64_t rows) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint32_t* po = reinterpret_cast<const uint32_t*>(o) + row * (D / 2);
+  const uint32_t* pd = reinterpret_cast<const uint32_t*>(d_o) + row * (D / 2);
+  float acc = 0.f;
+#pragma unroll
+  for (int i = lane; i < D / 2; i += 32) {
+    float a0, a1, b0, b1;
+    unpack2<ET == kBF16>(po[i], a0, a1);
+    unpack2<ET == kBF16>(pd[i], b0, b1);
+    acc = fmaf(a0, b0, fmaf(a1, b1, acc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// dq (16-bit) = dq_accum (fp32), four elements per thread.
+template <int ET>
+__global__ void __launch_bounds__(256) fmha_bwd_dq_kernel(const float* acc, void* dq, int64_t n) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i >= n) return;
+  const float4 a = *reinterpret_cast<const float4*>(acc + i);
+  uint2 out;
+  out.x = pack2<ET == kBF16>(a.x, a.y);
+  out.y = pack2<ET == kBF16>(a.z, a.w);
+  *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(dq) + i) = out;
+}
+
 }  // namespace wsa

@@ -9,6 +9,7 @@
 namespace wsa {
 
 struct FwdParams;
+struct BwdParams;
 
 // Enqueue the forward kernel for one (head dim, dtype, mask) variant.
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -22,5 +23,14 @@ cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap& tq, const
 cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tvt, const FwdParams& prm, unsigned grid,
                             cudaStream_t stream);
+
+// Backward pass (16-bit, D = 64 or 128): the main kernel over (head, key
+// block), the delta pre-pass over rows, and the dQ conversion of n elements.
+cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const BwdParams& prm, unsigned grid, cudaStream_t stream);
+cudaError_t launch_bwd_delta(int D, bool bf16, const void* o, const void* d_o, float* delta,
+                             int64_t rows, cudaStream_t stream);
+cudaError_t launch_bwd_dq(bool bf16, const float* acc, void* dq, int64_t n, cudaStream_t stream);
 
 }  // namespace wsa

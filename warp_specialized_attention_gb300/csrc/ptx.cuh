@@ -492,6 +492,22 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Two 16-bit values (lo in bits 0-15) to fp32, exactly.
+template <bool BF16>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+  if constexpr (BF16) {
+    lo = __uint_as_float(v << 16);
+    hi = __uint_as_float(v & 0xffff0000u);
+  } else {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
+  }
+}
+
 // Four fp32 values rounded to nearest-even E4M3 (saturating to +-448) and
 // packed, `a` in bits 0-7 (the element order of an 8-bit MMA operand in a
 // TMEM column).
