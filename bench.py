@@ -21,6 +21,12 @@ ours (default):
             workload on this host's cores (rank 0, N=1 only).
 reference:  the fp64 CPU oracle itself, timed the same way on bounded samples.
 
+--pass bwd times the backward pass (fmha_bwd) instead: a step is one backward
+over the workload given the forward's O and LSE, counted as 2.5x the forward
+FLOPs (five products of 2*S^2*D per head instead of two); its e2e leg copies
+Q, K, V, O, LSE, dO in from pinned host memory and dQ, dK, dV out per step,
+and its CPU baseline is the fp64 backward oracle on one (batch, head) slice.
+
 Under torchrun (N > 1) every rank runs its own copy of the workload (the
 (batch, head) units are independent, so per-GPU work is fixed: weak scaling);
 there is no data-path collective, only a barrier and a max of the timings.
@@ -52,6 +58,7 @@ METRIC = "FMHA fwd TFLOPS at B4 H32 S16K D128 fp16; % of GB300 dense tensor peak
 UNIT = "TFLOPS"
 KERNEL_SOURCES = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu",
                   "fmha_fwd_e4m3.cu", "fmha_api.cu"]
+BWD_SOURCES = ["fmha_bwd_sm103.cuh", "fmha_bwd.cu"]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -109,15 +116,15 @@ def _peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
 
 
-def _kernel_sha():
+def _kernel_sha(sources=None):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, "warp_specialized_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def _traffic(workload_name):
+def _traffic(workload_name, sources=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -126,7 +133,7 @@ def _traffic(workload_name):
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload_name)
-    if not e or e.get("kernel_sha") != _kernel_sha():
+    if not e or e.get("kernel_sha") != _kernel_sha(sources):
         return None
     return e.get("bytes_per_launch")
 
@@ -425,6 +432,122 @@ def run_ours(args, w):
     return 0
 
 
+def run_ours_bwd(args, w):
+    import oracle
+    import warp_specialized_attention_gb300 as wsa
+    world, rank, local = _dist_env()
+    dist = _init_dist(world)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the attention path has no CPU fallback)")
+    if w.dtype == "e4m3":
+        raise SystemExit("the backward pass takes 16-bit inputs")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wsa.load_library()
+    q, k, v = synthetic.make_inputs_device(w, device, seed=rank_seed(w, rank))
+    g = torch.Generator(device=device)
+    g.manual_seed(rank_seed(w, rank) + 1)
+    d_o = torch.randn(q.shape, generator=g, device=device, dtype=torch.float32).to(q.dtype)
+    o, lse = wsa.attention(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(wsa.fmha_bwd_workspace_bytes(w.B, w.H, w.S, w.D), dtype=torch.uint8,
+                     device=device)
+    stream = torch.cuda.current_stream(device)
+    step = lambda: wsa.fmha_bwd(q, k, v, o, lse, d_o, dq, dk, dv, workspace=ws,  # noqa: E731
+                                causal=w.causal, scale=w.scale, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    if wsa.get_device_status(stream) != wsa.FMHA_OK:
+        raise SystemExit("device status error after warm-up")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(device) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    _barrier(dist, device)
+    torch.cuda.synchronize(device)
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    _barrier(dist, device)
+    clocks = sampler.stop() if sampler else None
+    launches = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = _max_over_ranks(dist, ev[0].elapsed_time(ev[-1]), device)
+    if wsa.get_device_status(stream) != wsa.FMHA_OK:
+        raise SystemExit("device status error in the timed region")
+    flops = 2.5 * w.flops
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step / 1e3) / 1e12
+    step_ms = statistics.mean(launches)
+    achieved = flops / (step_ms / 1e3) / 1e12
+
+    # e2e: inputs in from pinned host memory, gradients out, every step
+    hin = [t.cpu().pin_memory() for t in (q, k, v, o, lse, d_o)]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    din = (q, k, v, o, lse, d_o)
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dt_, ht in zip(din, hin):
+                dt_.copy_(ht, non_blocking=True)
+            step()
+            for ht, dt_ in zip(hout, (dq, dk, dv)):
+                ht.copy_(dt_, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = _max_over_ranks(dist, e0.elapsed_time(e1), device) / e2e_steps
+    if not all(torch.isfinite(t[0, 0, :4].float()).all().item() for t in hout):
+        raise SystemExit("end-to-end gradients are not finite")
+
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qh, kh, vh, doh = (t[0, 0].double().cpu().numpy() for t in (q, k, v, d_o))
+        t0 = time.perf_counter()
+        oracle.attention_bwd(qh, kh, vh, doh, w.causal, w.scale)
+        dt = time.perf_counter() - t0
+        cpu = {"value": 2.5 * w.flops / (w.B * w.H) / dt / 1e12, "unit": UNIT,
+               "cores": oracle.threads(), "kind": "oracle",
+               "sample": "one whole (batch, head) slice of %s, backward oracle, %.2f s"
+                         % (w.describe(), dt)}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "FMHA bwd TFLOPS (2.5x forward FLOPs) at %s" % w.describe(), "value": value,
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(_config(w), **{"pass": "backward"}),
+        "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
+                "ms_per_step": e2e_ms, "api": "pinned host copies + fmha_bwd on one stream"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": _traffic(w.name + "_bwd", KERNEL_SOURCES + BWD_SOURCES),
+                     "peak_source": "%s bf16 burst dense (fp16 nominal ratio 1)" % peak_src,
+                     "step_ms_mean": step_ms, "step_ms_min": min(launches),
+                     "note": "a step is 4 launches (memset, delta, backward, dQ conversion)"},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,6 +561,8 @@ def main(argv=None):
                     help="(batch, head) chunks for the end-to-end leg (0: library default)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (smaller profiling captures)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward pass")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
     w = synthetic.by_name(args.workload)
@@ -445,6 +570,8 @@ def main(argv=None):
         w = dataclasses.replace(w, B=args.batch, name="%s_b%d" % (w.name, args.batch))
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 
