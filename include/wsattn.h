@@ -166,6 +166,30 @@ fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o,
                      int causal, float scale, fmha_dtype dtype, void* stream);
 
 /*
+ * fmha_bwd_noalloc -- fmha_bwd without a workspace argument: the dQ
+ * accumulator and delta live in a device array of the library (96 MiB, one
+ * per device), so the call needs no memory from the caller or an allocator.
+ * The pages have no counterpart; it serves callers that cannot provide
+ * scratch (a fixed memory budget, or a graph captured once and replayed).
+ *
+ *   Arguments as fmha_bwd, minus workspace and workspace_bytes.
+ *   Capacity: B*H*S*(4*D + 4) bytes must fit in 96 MiB (B*H*S <= 195,084
+ *   rows at D = 128, <= 387,166 at D = 64); larger inputs return
+ *   FMHA_ERR_UNSUPPORTED before any CUDA call, as do E4M3 inputs.
+ *   Races: every call on a device uses the same array, so calls whose work
+ *   overlaps in time (different streams, or several host threads) corrupt
+ *   each other's dQ; serialise them (one stream, or events).
+ *   Set-up: the first call on a device looks up the array's address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture,
+ *   and capture later calls freely.
+ * Errors as fmha_bwd.
+ */
+fmha_status fmha_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                             int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                             fmha_dtype dtype, void* stream);
+
+/*
  * fmha_get_device_status -- synchronise `stream`, then report and clear the
  * device status word of the current device.  Returns FMHA_ERR_TIMEOUT if any
  * kernel since the previous call abandoned a wait, FMHA_ERR_CUDA if the stream

@@ -157,6 +157,24 @@ def test_e4m3_overlap_uses_the_byte_sizes(lib):
         assert _call(lib, [q, k, v, q + n, lse], dtype=wsa.FMHA_E4M3) == wsa.FMHA_ERR_CUDA
 
 
+def test_noalloc_backward_rejects_what_its_scratch_cannot_hold(lib):
+    """fmha_bwd_noalloc checks its capacity (96 MiB: B*H*S*(4D + 4) bytes) on
+    the host, before any CUDA call."""
+    q, k, v, o, lse = _ptrs()
+    args = (q, k, v, o, lse, _BASE + 5 * (1 << 30), _BASE + 6 * (1 << 30), _BASE + 7 * (1 << 30),
+            _BASE + 8 * (1 << 30))
+    cap_rows = (96 << 20) // (4 * 128 + 4)                       # 195,084 at D = 128
+    assert lib.fmha_bwd_noalloc(*args, 1, 1, cap_rows + 1, 128, 0, 0.088, 0, None) == \
+        wsa.FMHA_ERR_UNSUPPORTED
+    assert lib.fmha_bwd_noalloc(*args, 1, 1, 128, 128, 0, 0.088, wsa.FMHA_E4M3, None) == \
+        wsa.FMHA_ERR_UNSUPPORTED
+    assert lib.fmha_bwd_noalloc(*args, 0, 1, 128, 128, 0, 0.088, 0, None) == \
+        wsa.FMHA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():   # within capacity: validation passes, CUDA is missing
+        assert lib.fmha_bwd_noalloc(*args, 1, 1, cap_rows, 128, 0, 0.088, 0, None) == \
+            wsa.FMHA_ERR_CUDA
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     assert _call(lib) == wsa.FMHA_ERR_CUDA

@@ -25,7 +25,7 @@ __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
     "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
-    "fmha_bwd", "fmha_bwd_workspace_bytes", "attention_backward",
+    "fmha_bwd", "fmha_bwd_workspace_bytes", "fmha_bwd_noalloc", "attention_backward",
     "get_device_status", "status_str", "version",
 ]
 
@@ -81,6 +81,9 @@ def load_library():
         lib.fmha_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t, i64, i64, i64, i64, ctypes.c_int,
                                              ctypes.c_float, ctypes.c_int, vp]
         lib.fmha_bwd.restype = ctypes.c_int
+        lib.fmha_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i64, i64, ctypes.c_int,
+                                                    ctypes.c_float, ctypes.c_int, vp]
+        lib.fmha_bwd_noalloc.restype = ctypes.c_int
         lib.fmha_get_device_status.argtypes = [vp]
         lib.fmha_get_device_status.restype = ctypes.c_int
         lib.fmha_status_str.argtypes = [ctypes.c_int]
@@ -264,6 +267,29 @@ def fmha_bwd(q, k, v, o, lse, d_o, dq, dk, dv, workspace=None, causal: bool = Fa
                           _stream_handle(stream))
     if st != FMHA_OK:
         raise FmhaError(st, "fmha_bwd", lib.fmha_last_cuda_error().decode())
+
+
+def fmha_bwd_noalloc(q, k, v, o, lse, d_o, dq, dk, dv, causal: bool = False,
+                     scale: float | None = None, stream=None) -> None:
+    """fmha_bwd with the library's own static scratch (C ABI fmha_bwd_noalloc):
+    no workspace, a size limit, and calls that overlap in time race."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    for name, t in (("d_o", d_o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("%s must match q's shape and dtype" % name)
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        st = lib.fmha_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), d_o.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), B, H, S, D, int(bool(causal)), float(scale),
+                                  _dtype_code(q), _stream_handle(stream))
+    if st != FMHA_OK:
+        raise FmhaError(st, "fmha_bwd_noalloc", lib.fmha_last_cuda_error().decode())
 
 
 def attention_backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None,

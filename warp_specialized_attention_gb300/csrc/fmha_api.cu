@@ -417,6 +417,26 @@ fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o,
                   causal, scale, static_cast<int>(dtype), stream, kDefaultWaitLimitNs);
 }
 
+fmha_status fmha_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                             int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
+                             fmha_dtype dtype, void* stream) {
+  // host checks first (no CUDA call): the arguments as fmha_bwd takes them,
+  // then the capacity of the static scratch, B*H*S rows of (4D + 4) bytes
+  // (B*H < 2^31 and S < 2^31 once validated, so the product fits in 64 bits)
+  const fmha_status vs = validate(q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, H,
+                                  S, D, scale, static_cast<int>(dtype));
+  if (vs != FMHA_OK) return vs;
+  if (dtype == FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
+  const int64_t cap_rows = static_cast<int64_t>(wsa::kBwdStaticScratchBytes / (4 * D + 4));
+  if (B * H * S > cap_rows) return FMHA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const cudaError_t e = wsa::bwd_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(backward scratch)");
+  return bwd_impl(q, k, v, o, lse, d_o, dq, dk, dv, scratch, wsa::kBwdStaticScratchBytes, B, H,
+                  S, D, causal, scale, static_cast<int>(dtype), stream, kDefaultWaitLimitNs);
+}
+
 fmha_status fmha_get_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

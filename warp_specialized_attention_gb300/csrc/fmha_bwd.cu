@@ -10,6 +10,11 @@ namespace wsa {
 
 namespace {
 
+// Scratch of the allocation-free backward entry point: the dQ accumulator and
+// delta (B*H*S*(4D + 4) bytes) in a file-scope device array, so a call needs
+// no memory from anyone.  Every call on this device shares it.
+__device__ __align__(256) unsigned char g_bwd_scratch[kBwdStaticScratchBytes];
+
 template <int D, int ET, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& prm, unsigned grid,
@@ -44,6 +49,25 @@ cudaError_t launch_bwd_d(bool bf16, bool causal, const CUtensorMap& tq, const CU
 }
 
 }  // namespace
+
+cudaError_t bwd_static_scratch(void** out) {
+  // looked up once per device (the first call, which should precede any
+  // stream capture); later calls only read the cache
+  constexpr int kMaxDevices = 64;
+  static std::atomic<void*> cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
 
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,

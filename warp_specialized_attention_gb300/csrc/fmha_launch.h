@@ -33,4 +33,9 @@ cudaError_t launch_bwd_delta(int D, bool bf16, const void* o, const void* d_o, f
                              int64_t rows, cudaStream_t stream);
 cudaError_t launch_bwd_dq(bool bf16, const float* acc, void* dq, int64_t n, cudaStream_t stream);
 
+// Capacity of the file-scope scratch of the allocation-free backward entry
+// point, and its device address (looked up once per device).
+constexpr size_t kBwdStaticScratchBytes = size_t{96} << 20;
+cudaError_t bwd_static_scratch(void** out);
+
 }  // namespace wsa
