@@ -33,7 +33,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+  kern<<<grid, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
   return cudaGetLastError();
 }
 

@@ -46,19 +46,37 @@ __device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_lo, uint
   }
 }
 
+// dV += P^T dO with P^T from TMEM (TMEM-A form, dO MN-major), the P^T of
+// queries 0-63 at columns [0, 32) and of queries 64-127 at [64, 96): each half
+// is written by its own warps over S^T columns that only those warps read.
+template <int D, int ET>
+__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint32_t do_lo,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = idesc_f16(ET == kBF16, 128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts_warp(d_tmem, p_tmem + kk * 8 + (kk >= 4 ? 32 : 0),
+                sdesc_join(do_lo + kk * ((16 * 128) >> 4), kDescHi), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
 // ============================================================================ the kernel
 //
-// Attention backward for one (head, 128-key block) per block of 320 threads:
-//   warps 0-3  dS / P: key row 32w + lane; read S^T and dP^T from TMEM, write
-//              P^T (16-bit) over S^T in TMEM and dS^T to shared memory; at the
-//              end write dK and dV
-//   warps 4-7  dQ: query row 32(w-4) + lane; read each block's dQ part from
+// Attention backward for one (head, 128-key block) per block of 448 threads:
+//   warps 0-7  dS / P: key row 32(w % 4) + lane, query columns 64(w / 4) ..
+//              +63 (two warps per SM sub-partition split the block's
+//              columns); read S^T and dP^T from TMEM, write P^T (16-bit) over
+//              S^T in TMEM and dS^T to shared memory; at the end write dV
+//              (w < 4) or dK (w >= 4)
+//   warps 8-11 dQ: query row 32(w % 4) + lane; read each block's dQ part from
 //              TMEM and add it, scaled, into the fp32 accumulator in global
 //              memory (vector red.add: several key blocks add into one row)
-//   warp 8     TMEM allocation and the tcgen05.mma issuer
-//   warp 9     TMA producer: K, V once; Q, dO per query block; LSE and delta
+//   warp 12    TMEM allocation and the tcgen05.mma issuer
+//   warp 13    TMA producer: K, V once; Q, dO per query block; LSE and delta
 // Per query block the issuer runs S^T = K Q^T, dP^T = V dO^T, then (once P^T
-// and dS^T are in place) dV += P^T dO, dK += dS^T Q and dQ = dS K.  The
+// and dS^T are in place) dV += P^T dO, dK += dS^T Q and dQ = dS K.  Each
+// half of the compute warps writes its P^T over S^T columns only it reads
+// (queries 0-63 to columns 0-31, 64-127 to 64-95; issue_dv reads them there).  The
 // chain-rule arithmetic is that of the backward oracle:
 //   P = exp(scale q.k - LSE), dS = P (dP - delta), delta_i = dO_i . O_i,
 //   dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K.
@@ -66,6 +84,10 @@ __device__ __forceinline__ void issue_mn_mn(uint32_t d_tmem, uint32_t a_lo, uint
 // Section III-B/III-E); every wait is bounded and raises the abort flag.
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kBwdThreads = 448;
+constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdWarpMma = 12;
+constexpr int kBwdWarpLoad = 13;
 
 template <int D>
 struct BwdCfg {
@@ -139,7 +161,7 @@ __device__ __forceinline__ void tmem_ld_wait_x16(uint32_t (&r)[16]) {
 }
 
 template <int D, int ET, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     fmha_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -169,10 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.do_free, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.stat_full[i], 1);
-      mbar_init(&ctl.stat_free[i], 4);
+      mbar_init(&ctl.stat_free[i], kBwdComputeWarps);
     }
     mbar_init(&ctl.sd_full, 1);
-    mbar_init(&ctl.p_ready, 4);
+    mbar_init(&ctl.p_ready, kBwdComputeWarps);
     mbar_init(&ctl.ds_free, 1);
     mbar_init(&ctl.dq_full, 1);
     mbar_init(&ctl.dq_free, 4);
@@ -181,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl.abort = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kBwdWarpMma) {
     tmem_alloc(&ctl.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -197,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, good);
   };
 
-  if (warp == kWarpLoad) {
+  if (warp == kBwdWarpLoad) {
     // ================================================================ TMA producer
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -245,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&ctl.do_full, (ndo_loads - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
                 p.wait_limit_ns);
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == kBwdWarpMma) {
     // ================================================================ MMA issuer
     const uint32_t k_lo = sdesc_lo(sK, kLboKMajor), v_lo = sdesc_lo(sV, kLboKMajor);
     const uint32_t q_lo = sdesc_lo(sQ, kLboKMajor), do_lo = sdesc_lo(sDO, kLboKMajor);
@@ -266,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_warp(&ctl.sd_full);
       if (!(ok = wait(&ctl.p_ready, n & 1, kStatusTimeoutMma))) break;
       tc_fence_after();
-      issue_pv<D, ET>(tmem + C::kColDV, tmem + C::kColS, do_mn, n > 0);  // dV += P^T dO
+      issue_dv<D, ET>(tmem + C::kColDV, tmem + C::kColS, do_mn, n > 0);  // dV += P^T dO
       issue_kmaj_mn<D, ET>(tmem + C::kColDK, ds_k, q_mn, n > 0);        // dK += dS^T Q
       mma_commit_warp(&ctl.q_free);
       mma_commit_warp(&ctl.do_free);
@@ -278,12 +300,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit_warp(&ctl.mma_drain);
     mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < kBwdComputeWarps) {
     // ================================================================ P and dS (key rows)
-    const int r = warp * 32 + lane;  // key row in the block, TMEM lane
+    const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+    const int r = quad * 32 + lane;               // key row in the block, TMEM lane
     const int key = kb * 128 + r;
     const bool key_ok = key < S;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float cl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; ok && n < nq; ++n) {
@@ -298,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* dl = lse2 + 128;
       const bool diag = CAUSAL && qb == kb;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {  // 16 queries per chunk
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {  // 16 queries per chunk
         uint32_t sv[16], dpv[16];
         tmem_ld_x16_async(lane_base + C::kColS + c * 16, sv);
         tmem_ld_x16_async(lane_base + C::kColDP + c * 16, dpv);
@@ -319,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
           dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
         }
-        tmem_st_x8_async(lane_base + C::kColS + c * 8, pk);  // P^T over S^T
+        // P^T over S^T columns this warp has read: queries 16c.. at column
+        // 8c (first half) or 8c + 32 (second half, see issue_dv)
+        tmem_st_x8_async(lane_base + C::kColS + c * 8 + half * 32, pk);
         // dS^T row r, queries 16c..16c+15: two 16-byte units of the
         // 128-byte-swizzled tile (unit index XOR row % 8)
         const uint32_t cb = c >> 2, u0 = (c & 3) * 2;
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const size_t row_off = (static_cast<size_t>(bh) * S + (key_ok ? key : 0)) * D * 2;
 #pragma unroll 1
-      for (int t = 0; t < 2; ++t) {
+      for (int t = half; t < half + 1; ++t) {  // dV from the first half, dK from the second
         uint8_t* out = reinterpret_cast<uint8_t*>(t ? p.dk : p.dv) + row_off;
         const float mul = t ? p.scale : 1.f;
         const uint32_t col = t ? C::kColDK : C::kColDV;
@@ -404,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: every role has drained its asynchronous work
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kBwdWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
