@@ -93,8 +93,9 @@ template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kTile = 128 * D * 2;                // 128 rows x D, 16-bit
-  static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 3 * kTile;
-  static constexpr int kOffDS = 4 * kTile;                 // dS^T, 128 x 128 16-bit
+  // K, V, two Q buffers, dO, dS^T
+  static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile;
+  static constexpr int kOffDS = 5 * kTile;                 // dS^T, 128 x 128 16-bit
   static constexpr int kOffStat = kOffDS + 128 * 128 * 2;  // 2 x (LSE*log2e[128], delta[128])
   static constexpr int kOffCtl = kOffStat + 2 * 256 * 4;
   static constexpr int kSmemBytes = 1024 + kOffCtl + 256;
@@ -105,7 +106,7 @@ struct BwdCfg {
 
 struct BwdCtl {
   uint64_t kv_full;
-  uint64_t q_full, q_free, do_full, do_free;
+  uint64_t q_full[2], q_free[2], do_full, do_free;
   uint64_t stat_full[2], stat_free[2];
   uint64_t sd_full;   // S^T and dP^T are in TMEM
   uint64_t p_ready;   // P^T in TMEM and dS^T in shared memory
@@ -182,11 +183,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int kb = blockIdx.x - bh * p.n_blk;
   const int qb0 = CAUSAL ? kb : 0;       // query blocks that see this key block
   const int nq = p.n_blk - qb0;          // >= 1
+  // The n-th query block of this key block.  Without the mask every key block
+  // starts at its own index and wraps around, so that the blocks of a head
+  // running side by side add into different dQ rows (with the mask key block
+  // kb starts at query block kb, which already spreads them).
+  auto qblock = [&](int n) {
+    int qb = qb0 + n;
+    if (!CAUSAL) {
+      qb += kb;
+      if (qb >= p.n_blk) qb -= p.n_blk;
+    }
+    return qb;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl.kv_full, 1);
-    mbar_init(&ctl.q_full, 1);
-    mbar_init(&ctl.q_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.q_full[i], 1);
+      mbar_init(&ctl.q_free[i], 1);
+    }
     mbar_init(&ctl.do_full, 1);
     mbar_init(&ctl.do_free, 1);
     for (int i = 0; i < 2; ++i) {
@@ -233,11 +248,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     int nq_loads = 0, ndo_loads = 0;  // Q and dO tiles issued
     for (int n = 0; n < nq; ++n) {
-      const int qb = qb0 + n;
-      if (n >= 1 && !wait(&ctl.q_free, (n - 1) & 1, kStatusTimeoutLoad)) break;
-      mbar_arrive_expect_tx_warp(&ctl.q_full, C::kTile);
+      const int qb = qblock(n);
+      // Q: two buffers, so the next block's Q loads while this one computes
+      const int qbuf = n & 1;
+      if (n >= 2 && !wait(&ctl.q_free[qbuf], ((n >> 1) - 1) & 1, kStatusTimeoutLoad)) break;
+      mbar_arrive_expect_tx_warp(&ctl.q_full[qbuf], C::kTile);
       for (int cb = 0; cb < D / 64; ++cb)
-        tma_load_3d_warp(sQ + cb * (128 * 128), &tm_q, &ctl.q_full, cb * 64, qb * 128, bh, pol_q);
+        tma_load_3d_warp(sQ + qbuf * C::kTile + cb * (128 * 128), &tm_q, &ctl.q_full[qbuf],
+                         cb * 64, qb * 128, bh, pol_q);
       ++nq_loads;
       if (n >= 1 && !wait(&ctl.do_free, (n - 1) & 1, kStatusTimeoutLoad)) break;
       mbar_arrive_expect_tx_warp(&ctl.do_full, C::kTile);
@@ -260,9 +278,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     // Drain: every issued copy lands before the block may exit.
     mbar_wait(&ctl.kv_full, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
-    if (nq_loads > 0)
-      mbar_wait(&ctl.q_full, (nq_loads - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
-                p.wait_limit_ns);
+    for (int b = 0; b < 2; ++b) {  // loads into buffer b: n = b, b + 2, ...
+      const int nb = (nq_loads + 1 - b) >> 1;
+      if (nb > 0)
+        mbar_wait(&ctl.q_full[b], (nb - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
+                  p.wait_limit_ns);
+    }
     if (ndo_loads > 0)
       mbar_wait(&ctl.do_full, (ndo_loads - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
                 p.wait_limit_ns);
@@ -270,13 +291,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdWarpMma) {
     // ================================================================ MMA issuer
     const uint32_t k_lo = sdesc_lo(sK, kLboKMajor), v_lo = sdesc_lo(sV, kLboKMajor);
-    const uint32_t q_lo = sdesc_lo(sQ, kLboKMajor), do_lo = sdesc_lo(sDO, kLboKMajor);
-    const uint32_t k_mn = sdesc_lo(sK, kLboV), q_mn = sdesc_lo(sQ, kLboV);
+    const uint32_t do_lo = sdesc_lo(sDO, kLboKMajor);
+    const uint32_t k_mn = sdesc_lo(sK, kLboV);
     const uint32_t do_mn = sdesc_lo(sDO, kLboV);
     const uint32_t ds_k = sdesc_lo(sDS, kLboKMajor), ds_mn = sdesc_lo(sDS, kLboV);
     bool ok = wait(&ctl.kv_full, 0, kStatusTimeoutMma);
     for (int n = 0; ok && n < nq; ++n) {
-      ok = wait(&ctl.q_full, n & 1, kStatusTimeoutMma) &&
+      const int qbuf = n & 1;
+      const uint32_t q_lo = sdesc_lo(sQ + qbuf * C::kTile, kLboKMajor);
+      const uint32_t q_mn = sdesc_lo(sQ + qbuf * C::kTile, kLboV);
+      ok = wait(&ctl.q_full[qbuf], (n >> 1) & 1, kStatusTimeoutMma) &&
            wait(&ctl.do_full, n & 1, kStatusTimeoutMma);
       if (!ok) break;
       tc_fence_after();
@@ -289,9 +313,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!(ok = wait(&ctl.p_ready, n & 1, kStatusTimeoutMma))) break;
       tc_fence_after();
       issue_dv<D, ET>(tmem + C::kColDV, tmem + C::kColS, do_mn, n > 0);  // dV += P^T dO
-      issue_kmaj_mn<D, ET>(tmem + C::kColDK, ds_k, q_mn, n > 0);        // dK += dS^T Q
-      mma_commit_warp(&ctl.q_free);
       mma_commit_warp(&ctl.do_free);
+      issue_kmaj_mn<D, ET>(tmem + C::kColDK, ds_k, q_mn, n > 0);        // dK += dS^T Q
+      mma_commit_warp(&ctl.q_free[qbuf]);
       issue_mn_mn<D, ET>(tmem + C::kColDQ, ds_mn, k_mn, false);         // dQ part = dS K
       mma_commit_warp(&ctl.dq_full);
       mma_commit_warp(&ctl.ds_free);
@@ -310,7 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float cl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; ok && n < nq; ++n) {
-      const int qb = qb0 + n;
+      const int qb = qblock(n);
       const int buf = n & 1;
       ok = wait(&ctl.stat_full[buf], (n >> 1) & 1, kStatusTimeoutSoftmax) &&
            wait(&ctl.sd_full, n & 1, kStatusTimeoutSoftmax) &&
@@ -327,20 +351,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_x16_async(lane_base + C::kColDP + c * 16, dpv);
         tmem_ld_wait_x16(sv);
         tmem_ld_wait_x16(dpv);
-        uint32_t pk[16], dk16[8];
+        uint32_t pk[8], dk16[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float pp[2], dd[2];
+        for (int e = 0; e < 16; e += 4) {
+          // the four queries' statistics: one vector load each (broadcast)
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 16 + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 16 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], dd[4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 4; ++h) {
             const int qi = c * 16 + e + h;
             const bool vis = key_ok && !(diag && r > qi);
-            const float pv = vis ? ex2(__uint_as_float(sv[e + h]) * cl2 - lse2[qi]) : 0.f;
+            const float pv = vis ? ex2(__uint_as_float(sv[e + h]) * cl2 - lv[h]) : 0.f;
             pp[h] = pv;
-            dd[h] = pv * (__uint_as_float(dpv[e + h]) - dl[qi]);
+            dd[h] = pv * (__uint_as_float(dpv[e + h]) - dv4[h]);
           }
           pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
+          pk[(e >> 1) + 1] = pack2<ET == kBF16>(pp[2], pp[3]);
           dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
+          dk16[(e >> 1) + 1] = pack2<ET == kBF16>(dd[2], dd[3]);
         }
         // P^T over S^T columns this warp has read: queries 16c.. at column
         // 8c (first half) or 8c + 32 (second half, see issue_dv)
@@ -403,7 +433,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     bool ok = true;
     for (int n = 0; ok && n < nq; ++n) {
-      const int q = (qb0 + n) * 128 + quad * 32 + lane;
+      const int q = qblock(n) * 128 + quad * 32 + lane;
       if (!(ok = wait(&ctl.dq_full, n & 1, kStatusTimeoutSoftmax))) break;
       tc_fence_after();
       float* dst = p.dq_accum + (static_cast<size_t>(bh) * S + (q < S ? q : 0)) * D;

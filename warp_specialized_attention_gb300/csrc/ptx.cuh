@@ -415,7 +415,9 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 // tcgen05.st 32 lanes x 32 bits, 8 consecutive columns (r[0..7]), no wait.
-__device__ __forceinline__ void tmem_st_x8_async(uint32_t taddr, const uint32_t (&r)[16]) {
+template <int N>
+__device__ __forceinline__ void tmem_st_x8_async(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N >= 8, "eight registers");
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
                   "r"(r[6]), "r"(r[7])
