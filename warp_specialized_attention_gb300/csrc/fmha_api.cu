@@ -84,6 +84,22 @@ bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype,
   return r == CUDA_SUCCESS;
 }
 
+// The backward's fp32 dQ accumulator (B*H, S, D): boxes of 32 rows x 16
+// columns (64 bytes), 64-byte swizzle, for the kernel's TMA reduce-adds.
+bool encode_dq_map(EncodeTiledFn enc, CUtensorMap* map, float* ptr, int64_t BH, int64_t S,
+                   int64_t D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 4),
+                                 static_cast<cuuint64_t>(S * D * 4)};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Bytes per element of the inputs and of O.
 size_t in_bytes(int dtype) { return dtype == FMHA_E4M3 ? 1 : 2; }
 constexpr size_t kOutBytes = 2;
@@ -247,6 +263,9 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   const bool bf16 = dtype == FMHA_BF16;
   float* dq_acc = static_cast<float*>(workspace);
   float* delta = dq_acc + static_cast<size_t>(BH * S * D);
+  alignas(64) CUtensorMap tdq;
+  if (!encode_dq_map(enc, &tdq, dq_acc, BH, S, D))
+    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(dQ accumulator)");
   if ((e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(BH * S * D) * 4, st)) != cudaSuccess)
     return cuda_fail(e, "clear the dQ accumulator");
   if ((e = wsa::launch_bwd_delta(static_cast<int>(D), bf16, o, d_o, delta, BH * S, st)) !=
@@ -264,7 +283,7 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   prm.scale = scale;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.wait_limit_ns = wait_limit_ns;
-  if ((e = wsa::launch_bwd(static_cast<int>(D), bf16, causal != 0, tq, tk, tv, tdo, prm,
+  if ((e = wsa::launch_bwd(static_cast<int>(D), bf16, causal != 0, tq, tk, tv, tdo, tdq, prm,
                            static_cast<unsigned>(n_blk * BH), st)) != cudaSuccess)
     return cuda_fail(e, "backward kernel launch");
   if ((e = wsa::launch_bwd_dq(bf16, dq_acc, dq, BH * S * D, st)) != cudaSuccess)

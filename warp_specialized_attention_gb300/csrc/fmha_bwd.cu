@@ -17,8 +17,8 @@ __device__ __align__(256) unsigned char g_bwd_scratch[kBwdStaticScratchBytes];
 
 template <int D, int ET, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdParams& prm, unsigned grid,
-                         cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& prm,
+                         unsigned grid, cudaStream_t stream) {
   auto kern = fmha_bwd_kernel<D, ET, CAUSAL>;
   // Dynamic shared memory above 48 KB is opted into once per device (flags
   // private to this library copy: internal linkage).
@@ -33,19 +33,19 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, prm);
+  kern<<<grid, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_bwd_d(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& prm,
-                         unsigned grid, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                         const BwdParams& prm, unsigned grid, cudaStream_t stream) {
   if (bf16)
-    return causal ? launch_bwd_t<D, kBF16, true>(tq, tk, tv, tdo, prm, grid, stream)
-                  : launch_bwd_t<D, kBF16, false>(tq, tk, tv, tdo, prm, grid, stream);
-  return causal ? launch_bwd_t<D, kF16, true>(tq, tk, tv, tdo, prm, grid, stream)
-                : launch_bwd_t<D, kF16, false>(tq, tk, tv, tdo, prm, grid, stream);
+    return causal ? launch_bwd_t<D, kBF16, true>(tq, tk, tv, tdo, tdq, prm, grid, stream)
+                  : launch_bwd_t<D, kBF16, false>(tq, tk, tv, tdo, tdq, prm, grid, stream);
+  return causal ? launch_bwd_t<D, kF16, true>(tq, tk, tv, tdo, tdq, prm, grid, stream)
+                : launch_bwd_t<D, kF16, false>(tq, tk, tv, tdo, tdq, prm, grid, stream);
 }
 
 }  // namespace
@@ -71,9 +71,10 @@ cudaError_t bwd_static_scratch(void** out) {
 
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdParams& prm, unsigned grid, cudaStream_t stream) {
-  return D == 64 ? launch_bwd_d<64>(bf16, causal, tq, tk, tv, tdo, prm, grid, stream)
-                 : launch_bwd_d<128>(bf16, causal, tq, tk, tv, tdo, prm, grid, stream);
+                       const CUtensorMap& tdq, const BwdParams& prm, unsigned grid,
+                       cudaStream_t stream) {
+  return D == 64 ? launch_bwd_d<64>(bf16, causal, tq, tk, tv, tdo, tdq, prm, grid, stream)
+                 : launch_bwd_d<128>(bf16, causal, tq, tk, tv, tdo, tdq, prm, grid, stream);
 }
 
 cudaError_t launch_bwd_delta(int D, bool bf16, const void* o, const void* d_o, float* delta,

@@ -62,17 +62,19 @@ __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint3
 
 // ============================================================================ the kernel
 //
-// Attention backward for one (head, 128-key block) per block of 448 threads:
+// Attention backward for one (head, 128-key block) per block of 576 threads:
 //   warps 0-7  dS / P: key row 32(w % 4) + lane, query columns 64(w / 4) ..
 //              +63 (two warps per SM sub-partition split the block's
 //              columns); read S^T and dP^T from TMEM, write P^T (16-bit) over
 //              S^T in TMEM and dS^T to shared memory; at the end write dV
 //              (w < 4) or dK (w >= 4)
-//   warps 8-11 dQ: query row 32(w % 4) + lane; read each block's dQ part from
-//              TMEM and add it, scaled, into the fp32 accumulator in global
-//              memory (vector red.add: several key blocks add into one row)
-//   warp 12    TMEM allocation and the tcgen05.mma issuer
-//   warp 13    TMA producer: K, V once; Q, dO per query block; LSE and delta
+//   warps 8-15 dQ: query row 32(w % 4) + lane, columns D/2 (w - 8) / 4 ..
+//              +D/2; read each block's dQ part from TMEM into registers,
+//              release the columns, then pass it, scaled, through a 2 KB
+//              shared stage to a TMA reduce-add into the fp32 accumulator in
+//              global memory (several key blocks add into one row)
+//   warp 16    TMEM allocation and the tcgen05.mma issuer
+//   warp 17    TMA producer: K, V once; Q, dO per query block; LSE and delta
 // Per query block the issuer runs S^T = K Q^T, dP^T = V dO^T, then (once P^T
 // and dS^T are in place) dV += P^T dO, dK += dS^T Q and dQ = dS K.  Each
 // half of the compute warps writes its P^T over S^T columns only it reads
@@ -84,10 +86,11 @@ __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint3
 // Section III-B/III-E); every wait is bounded and raises the abort flag.
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBwdThreads = 448;
-constexpr int kBwdComputeWarps = 8;
-constexpr int kBwdWarpMma = 12;
-constexpr int kBwdWarpLoad = 13;
+constexpr int kBwdThreads = 576;
+constexpr int kBwdComputeWarps = 8;  // warps 0-7
+constexpr int kBwdDqWarps = 8;       // warps 8-15
+constexpr int kBwdWarpMma = 16;
+constexpr int kBwdWarpLoad = 17;
 
 template <int D>
 struct BwdCfg {
@@ -96,7 +99,10 @@ struct BwdCfg {
   // K, V, two Q buffers, dO, dS^T
   static constexpr int kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile;
   static constexpr int kOffDS = 5 * kTile;                 // dS^T, 128 x 128 16-bit
-  static constexpr int kOffStat = kOffDS + 128 * 128 * 2;  // 2 x (LSE*log2e[128], delta[128])
+  // dQ stages: one 2 KB tile (32 rows x 16 fp32, 64-byte swizzle) per dQ warp
+  static constexpr int kOffDQ = kOffDS + 128 * 128 * 2;
+  static constexpr int kDqStage = 32 * 16 * 4;
+  static constexpr int kOffStat = kOffDQ + kBwdDqWarps * kDqStage;  // 2 x (LSE*log2e, delta)
   static constexpr int kOffCtl = kOffStat + 2 * 256 * 4;
   static constexpr int kSmemBytes = 1024 + kOffCtl + 256;
   // TMEM columns: S^T (P^T over its first 64), dP^T (dQ reuses it), dV, dK
@@ -166,7 +172,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fmha_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   static_assert(ET != kE4M3, "backward: 16-bit inputs");
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&ctl.p_ready, kBwdComputeWarps);
     mbar_init(&ctl.ds_free, 1);
     mbar_init(&ctl.dq_full, 1);
-    mbar_init(&ctl.dq_free, 4);
+    mbar_init(&ctl.dq_free, kBwdDqWarps);
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.mma_drain, 1);
     ctl.abort = 0;
@@ -427,33 +434,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < kBwdComputeWarps + kBwdDqWarps) {
     // ================================================================ dQ (query rows)
-    const int quad = warp & 3;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    constexpr int kCols = D / 2;  // columns of this warp
+    const int quad = warp & 3, hc = (warp - kBwdComputeWarps) >> 2;
+    const uint32_t t_dq = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ + hc * kCols;
+    const uint32_t stage = sbase + C::kOffDQ + (warp - kBwdComputeWarps) * C::kDqStage;
+    if (lane == 0) prefetch_tmap(&tm_dq);
     bool ok = true;
     for (int n = 0; ok && n < nq; ++n) {
-      const int q = qblock(n) * 128 + quad * 32 + lane;
       if (!(ok = wait(&ctl.dq_full, n & 1, kStatusTimeoutSoftmax))) break;
       tc_fence_after();
-      float* dst = p.dq_accum + (static_cast<size_t>(bh) * S + (q < S ? q : 0)) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_x32(lane_base + C::kColDQ + ch * 32, r);
-        if (q < S) {
+      uint32_t r[kCols / 32][32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            red_add_v4(dst + ch * 32 + 4 * i, __uint_as_float(r[4 * i]) * p.scale,
-                       __uint_as_float(r[4 * i + 1]) * p.scale,
-                       __uint_as_float(r[4 * i + 2]) * p.scale,
-                       __uint_as_float(r[4 * i + 3]) * p.scale);
-        }
-      }
+      for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_x32_async(t_dq + ch * 32, r[ch]);
+#pragma unroll
+      for (int ch = 0; ch < kCols / 32; ++ch) tmem_ld_wait_x32(r[ch]);
+      // the columns are free for the next block's dP^T
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.dq_free);
+      // row q0 + lane of the box: 16 columns per stage, four 16-byte units at
+      // unit index XOR (row / 2) % 4 (the 64-byte swizzle)
+      // rows past S inside a box are skipped by the copy; boxes wholly past S
+      // are not issued
+      const int q0 = qblock(n) * 128 + quad * 32;
+      if (q0 >= S) continue;
+#pragma unroll
+      for (int sg = 0; sg < kCols / 16; ++sg) {
+        if (lane == 0) bulk_wait_group_read0();  // the stage's previous tile is read
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t a = stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4);
+          const uint32_t* f = &r[sg >> 1][(sg & 1) * 16 + 4 * u];
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                       "f"(__uint_as_float(f[0]) * p.scale), "f"(__uint_as_float(f[1]) * p.scale),
+                       "f"(__uint_as_float(f[2]) * p.scale), "f"(__uint_as_float(f[3]) * p.scale)
+                       : "memory");
+        }
+        fence_proxy_async_smem();  // the stores -> visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, stage, hc * kCols + sg * 16, q0, bh);
+          bulk_commit_group();
+        }
+      }
     }
+    if (lane == 0) bulk_wait_group0();  // every reduction has landed
+    __syncwarp();
   }
 
   // ---- teardown: every role has drained its asynchronous work

@@ -26,9 +26,12 @@ cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMa
 
 // Backward pass (16-bit, D = 64 or 128): the main kernel over (head, key
 // block), the delta pre-pass over rows, and the dQ conversion of n elements.
+// tdq maps the fp32 dQ accumulator (D, S, B*H) with 16 x 32 x 1 boxes and the
+// 64-byte swizzle.
 cudaError_t launch_bwd(int D, bool bf16, bool causal, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const BwdParams& prm, unsigned grid, cudaStream_t stream);
+                       const CUtensorMap& tdq, const BwdParams& prm, unsigned grid,
+                       cudaStream_t stream);
 cudaError_t launch_bwd_delta(int D, bool bf16, const void* o, const void* d_o, float* delta,
                              int64_t rows, cudaStream_t stream);
 cudaError_t launch_bwd_dq(bool bf16, const float* acc, void* dq, int64_t n, cudaStream_t stream);

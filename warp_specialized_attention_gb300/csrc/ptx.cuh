@@ -322,6 +322,36 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 3-D tiled bulk tensor reduction shared (this CTA) -> global: the tile at
+// src_smem is added element-wise into the box at (c0, c1, c2); elements of the
+// box outside the tensor are skipped.  Completion is tracked by the issuing
+// thread's bulk async-group (bulk_commit_group / bulk_wait_group_*), so the
+// same thread issues, commits and waits.  c0 x element size must be a
+// multiple of 16 bytes and no coordinate may be negative.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src_smem,
+                                                  int c0, int c1, int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src_smem), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every committed bulk group of this thread has finished reading
+// its shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until every committed bulk group of this thread is complete.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void clc_try_cancel_warp(uint32_t resp_smem, uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
