@@ -351,13 +351,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* lse2 = stats + buf * 256;
       const float* dl = lse2 + 128;
       const bool diag = CAUSAL && qb == kb;
-#pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; ++c) {  // 16 queries per chunk
-        uint32_t sv[16], dpv[16];
-        tmem_ld_x16_async(lane_base + C::kColS + c * 16, sv);
-        tmem_ld_x16_async(lane_base + C::kColDP + c * 16, dpv);
-        tmem_ld_wait_x16(sv);
-        tmem_ld_wait_x16(dpv);
+      // four chunks of 16 queries; chunk i + 1's S^T and dP^T loads are in
+      // flight while chunk i is computed (two register buffers, unrolled so
+      // that the buffers are indexed statically)
+      uint32_t sv[2][16], dpv[2][16];
+      tmem_ld_x16_async(lane_base + C::kColS + half * 64, sv[0]);
+      tmem_ld_x16_async(lane_base + C::kColDP + half * 64, dpv[0]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = 4 * half + i;
+        const int cur = i & 1;
+        tmem_ld_wait_x16(sv[cur]);
+        tmem_ld_wait_x16(dpv[cur]);
+        if (i < 3) {
+          tmem_ld_x16_async(lane_base + C::kColS + (c + 1) * 16, sv[cur ^ 1]);
+          tmem_ld_x16_async(lane_base + C::kColDP + (c + 1) * 16, dpv[cur ^ 1]);
+        }
         uint32_t pk[8], dk16[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -370,9 +379,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int h = 0; h < 4; ++h) {
             const int qi = c * 16 + e + h;
             const bool vis = key_ok && !(diag && r > qi);
-            const float pv = vis ? ex2(__uint_as_float(sv[e + h]) * cl2 - lv[h]) : 0.f;
+            const float pv = vis ? ex2(__uint_as_float(sv[cur][e + h]) * cl2 - lv[h]) : 0.f;
             pp[h] = pv;
-            dd[h] = pv * (__uint_as_float(dpv[e + h]) - dv4[h]);
+            dd[h] = pv * (__uint_as_float(dpv[cur][e + h]) - dv4[h]);
           }
           pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
           pk[(e >> 1) + 1] = pack2<ET == kBF16>(pp[2], pp[3]);
@@ -380,7 +389,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dk16[(e >> 1) + 1] = pack2<ET == kBF16>(dd[2], dd[3]);
         }
         // P^T over S^T columns this warp has read: queries 16c.. at column
-        // 8c (first half) or 8c + 32 (second half, see issue_dv)
+        // 8c (first half) or 8c + 32 (second half, see issue_dv); below the
+        // columns of the load in flight (16c + 16 and up)
         tmem_st_x8_async(lane_base + C::kColS + c * 8 + half * 32, pk);
         // dS^T row r, queries 16c..16c+15: two 16-byte units of the
         // 128-byte-swizzled tile (unit index XOR row % 8)
