@@ -17,6 +17,8 @@
 // 16 rows (2 KB), with the leading byte offset (16 KB) between 64-element
 // column blocks.
 #pragma once
+#include <type_traits>
+
 #include "fmha_fwd_sm103.cuh"
 
 namespace wsa {
@@ -270,15 +272,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d_warp(sDO + cb * (128 * 128), &tm_do, &ctl.do_full, cb * 64, qb * 128, bh,
                          pol_q);
       ++ndo_loads;
-      // this block's LSE (in log2 units) and delta; rows past S: P = 0
+      // this block's -LSE (in log2 units) and -delta, negated so that the
+      // compute warps add them; rows past S: P = 0
       const int buf = n & 1;
       if (n >= 2 && !wait(&ctl.stat_free[buf], ((n >> 1) - 1) & 1, kStatusTimeoutLoad)) break;
       float* st = stats + buf * 256;
       for (int r = lane; r < 128; r += 32) {
         const int q = qb * 128 + r;
         const size_t idx = static_cast<size_t>(bh) * S + q;
-        st[r] = q < S ? p.lse[idx] * kLog2e : INFINITY;
-        st[128 + r] = q < S ? p.delta[idx] : 0.f;
+        st[r] = q < S ? -(p.lse[idx] * kLog2e) : -INFINITY;
+        st[128 + r] = q < S ? -p.delta[idx] : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.stat_full[buf]);
@@ -337,6 +340,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int r = quad * 32 + lane;               // key row in the block, TMEM lane
     const int key = kb * 128 + r;
     const bool key_ok = key < S;
+    const bool key_ok_warp = __all_sync(0xffffffffu, key_ok);
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float cl2 = p.scale_log2;
     bool ok = true;
@@ -348,63 +352,110 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
            (n == 0 || wait(&ctl.ds_free, (n - 1) & 1, kStatusTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after();
-      const float* lse2 = stats + buf * 256;
-      const float* dl = lse2 + 128;
+      const float* nlse2 = stats + buf * 256;  // -LSE log2(e) per query
+      const float* ndl = nlse2 + 128;          // -delta per query
       const bool diag = CAUSAL && qb == kb;
-      // four chunks of 16 queries; chunk i + 1's S^T and dP^T loads are in
-      // flight while chunk i is computed (two register buffers, unrolled so
-      // that the buffers are indexed statically)
-      uint32_t sv[2][16], dpv[2][16];
-      tmem_ld_x16_async(lane_base + C::kColS + half * 64, sv[0]);
-      tmem_ld_x16_async(lane_base + C::kColDP + half * 64, dpv[0]);
+      // no key of any row of this warp is masked: the warp takes the packed
+      // path (warp-uniform, the tcgen05 loads and stores are warp-wide)
+      const bool plain = key_ok_warp && !diag;
+      // four chunks of 16 queries, in one of two instantiations (masked or
+      // not) so that each keeps its registers to itself
+      auto run_chunks = [&](auto kind) {
+        // four chunks of 16 queries; chunk i + 1's S^T and dP^T loads are in
+        // flight while chunk i is computed (two register buffers, unrolled so
+        // that the buffers are indexed statically)
+        uint32_t sv[2][16], dpv[2][16];
+        tmem_ld_x16_async(lane_base + C::kColS + half * 64, sv[0]);
+        tmem_ld_x16_async(lane_base + C::kColDP + half * 64, dpv[0]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int c = 4 * half + i;
-        const int cur = i & 1;
-        tmem_ld_wait_x16(sv[cur]);
-        tmem_ld_wait_x16(dpv[cur]);
-        if (i < 3) {
-          tmem_ld_x16_async(lane_base + C::kColS + (c + 1) * 16, sv[cur ^ 1]);
-          tmem_ld_x16_async(lane_base + C::kColDP + (c + 1) * 16, dpv[cur ^ 1]);
-        }
-        uint32_t pk[8], dk16[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          // the four queries' statistics: one vector load each (broadcast)
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c * 16 + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(dl + c * 16 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pp[4], dd[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int qi = c * 16 + e + h;
-            const bool vis = key_ok && !(diag && r > qi);
-            const float pv = vis ? ex2(__uint_as_float(sv[cur][e + h]) * cl2 - lv[h]) : 0.f;
-            pp[h] = pv;
-            dd[h] = pv * (__uint_as_float(dpv[cur][e + h]) - dv4[h]);
+        for (int i = 0; i < 4; ++i) {
+          const int c = 4 * half + i;
+          const int cur = i & 1;
+          tmem_ld_wait_x16(sv[cur]);
+          tmem_ld_wait_x16(dpv[cur]);
+          if (i < 3) {
+            tmem_ld_x16_async(lane_base + C::kColS + (c + 1) * 16, sv[cur ^ 1]);
+            tmem_ld_x16_async(lane_base + C::kColDP + (c + 1) * 16, dpv[cur ^ 1]);
           }
-          pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
-          pk[(e >> 1) + 1] = pack2<ET == kBF16>(pp[2], pp[3]);
-          dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
-          dk16[(e >> 1) + 1] = pack2<ET == kBF16>(dd[2], dd[3]);
+          uint32_t pk[8], dk16[8];
+          const uint32_t* sc = sv[cur];
+          const uint32_t* dpc = dpv[cur];
+          if constexpr (decltype(kind)::value) {
+            // P = 2^(s c - LSE log2 e) and dS = P (dP - delta), two queries per
+            // packed fp32x2 instruction; the same roundings as the masked path
+            const uint64_t c2 = f2_pack(cl2, cl2);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              // the four queries' statistics: one vector load each (broadcast)
+              const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c * 16 + e);
+              const float4 d4 = *reinterpret_cast<const float4*>(ndl + c * 16 + e);
+              float x[4];
+              f2_unpack(ffma2(f2_pack(__uint_as_float(sc[e]), __uint_as_float(sc[e + 1])), c2,
+                              f2_pack(l4.x, l4.y)), x[0], x[1]);
+              f2_unpack(ffma2(f2_pack(__uint_as_float(sc[e + 2]), __uint_as_float(sc[e + 3])), c2,
+                              f2_pack(l4.z, l4.w)), x[2], x[3]);
+              float pp[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) pp[h] = ex2(x[h]);
+              const uint64_t dd01 = fmul2(f2_pack(pp[0], pp[1]),
+                                          fadd2(f2_pack(__uint_as_float(dpc[e]),
+                                                        __uint_as_float(dpc[e + 1])),
+                                                f2_pack(d4.x, d4.y)));
+              const uint64_t dd23 = fmul2(f2_pack(pp[2], pp[3]),
+                                          fadd2(f2_pack(__uint_as_float(dpc[e + 2]),
+                                                        __uint_as_float(dpc[e + 3])),
+                                                f2_pack(d4.z, d4.w)));
+              float dd[4];
+              f2_unpack(dd01, dd[0], dd[1]);
+              f2_unpack(dd23, dd[2], dd[3]);
+              pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
+              pk[(e >> 1) + 1] = pack2<ET == kBF16>(pp[2], pp[3]);
+              dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
+              dk16[(e >> 1) + 1] = pack2<ET == kBF16>(dd[2], dd[3]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c * 16 + e);
+              const float4 d4 = *reinterpret_cast<const float4*>(ndl + c * 16 + e);
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pp[4], dd[4];
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const int qi = c * 16 + e + h;
+                const bool vis = key_ok && !(diag && r > qi);
+                const float pv = vis ? ex2(fmaf(__uint_as_float(sc[e + h]), cl2, lv[h])) : 0.f;
+                pp[h] = pv;
+                dd[h] = pv * (__uint_as_float(dpc[e + h]) + dv4[h]);
+              }
+              pk[e >> 1] = pack2<ET == kBF16>(pp[0], pp[1]);
+              pk[(e >> 1) + 1] = pack2<ET == kBF16>(pp[2], pp[3]);
+              dk16[e >> 1] = pack2<ET == kBF16>(dd[0], dd[1]);
+              dk16[(e >> 1) + 1] = pack2<ET == kBF16>(dd[2], dd[3]);
+            }
+          }
+          // P^T over S^T columns this warp has read: queries 16c.. at column
+          // 8c (first half) or 8c + 32 (second half, see issue_dv); below the
+          // columns of the load in flight (16c + 16 and up)
+          tmem_st_x8_async(lane_base + C::kColS + c * 8 + half * 32, pk);
+          // dS^T row r, queries 16c..16c+15: two 16-byte units of the
+          // 128-byte-swizzled tile (unit index XOR row % 8)
+          const uint32_t cb = c >> 2, u0 = (c & 3) * 2;
+          const uint32_t row_addr = sDS + cb * (128 * 128) + r * 128;
+          const uint32_t a0 = row_addr + ((u0 ^ (r & 7)) << 4);
+          const uint32_t a1 = row_addr + (((u0 + 1) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(dk16[0]),
+                       "r"(dk16[1]), "r"(dk16[2]), "r"(dk16[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(dk16[4]),
+                       "r"(dk16[5]), "r"(dk16[6]), "r"(dk16[7])
+                       : "memory");
         }
-        // P^T over S^T columns this warp has read: queries 16c.. at column
-        // 8c (first half) or 8c + 32 (second half, see issue_dv); below the
-        // columns of the load in flight (16c + 16 and up)
-        tmem_st_x8_async(lane_base + C::kColS + c * 8 + half * 32, pk);
-        // dS^T row r, queries 16c..16c+15: two 16-byte units of the
-        // 128-byte-swizzled tile (unit index XOR row % 8)
-        const uint32_t cb = c >> 2, u0 = (c & 3) * 2;
-        const uint32_t row_addr = sDS + cb * (128 * 128) + r * 128;
-        const uint32_t a0 = row_addr + ((u0 ^ (r & 7)) << 4);
-        const uint32_t a1 = row_addr + (((u0 + 1) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(dk16[0]),
-                     "r"(dk16[1]), "r"(dk16[2]), "r"(dk16[3])
-                     : "memory");
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(dk16[4]),
-                     "r"(dk16[5]), "r"(dk16[6]), "r"(dk16[7])
-                     : "memory");
-      }
+      };
+      if (plain)
+        run_chunks(std::true_type{});
+      else
+        run_chunks(std::false_type{});
       tmem_st_wait();
       fence_proxy_async_smem();  // dS^T stores -> visible to the tensor core
       tc_fence_before();
