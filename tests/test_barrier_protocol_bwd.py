@@ -12,7 +12,7 @@ mirrors the kernel's barrier program role by role:
            dO into its one buffer (do_full/do_free), LSE and delta into
            statistics buffer n % 2 (plain stores, stat_full/stat_free); then it
            waits for its own copies to land
-  MMA      S^T = K Q^T; after dq_free: dP^T = V dO^T, commit sd_full; after
+  MMA      S^T = K Q^T; after do_full and dq_free: dP^T = V dO^T, commit sd_full; after
            p_ready: dV (commit do_free), dK (commit q_free), dQ (commit dq_full,
            ds_free); at the end acc_done and its own drain
   compute  8 warps: statistics, S^T and dP^T in; P^T over S^T and dS^T out;
@@ -136,13 +136,13 @@ class BwdModel:
         for n in range(self.nq):
             qb = n & 1
             yield from self.wait(("q_full", qb), n >> 1)
-            yield from self.wait("do_full", n)
 
             def s_t(n=n, qb=qb):
                 self.expect("K", self.res["K"], "kv")
                 self.expect("Q buffer %d at S^T" % qb, self.res[("Q", qb)], ("Q", n))
                 self.s_cols = [("S", n)] * N_COMPUTE
             self.issue(s_t)
+            yield from self.wait("do_full", n)
             yield from self.mma_wait_dq_free(n)
 
             def dp_t(n=n):

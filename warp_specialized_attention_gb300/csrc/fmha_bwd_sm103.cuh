@@ -310,13 +310,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int qbuf = n & 1;
       const uint32_t q_lo = sdesc_lo(sQ + qbuf * C::kTile, kLboKMajor);
       const uint32_t q_mn = sdesc_lo(sQ + qbuf * C::kTile, kLboV);
-      ok = wait(&ctl.q_full[qbuf], (n >> 1) & 1, kStatusTimeoutMma) &&
-           wait(&ctl.do_full, n & 1, kStatusTimeoutMma);
-      if (!ok) break;
+      if (!(ok = wait(&ctl.q_full[qbuf], (n >> 1) & 1, kStatusTimeoutMma))) break;
       tc_fence_after();
       issue_qk<D, ET>(tmem + C::kColS, k_lo, q_lo);  // S^T = K Q^T
-      // dP^T takes the columns of the previous block's dQ part
-      if (n >= 1 && !(ok = wait(&ctl.dq_free, (n - 1) & 1, kStatusTimeoutMma))) break;
+      // dP^T needs this block's dO (one buffer, loaded once dV of the previous
+      // block has read it: S^T runs meanwhile) and takes the columns of the
+      // previous block's dQ part
+      ok = wait(&ctl.do_full, n & 1, kStatusTimeoutMma) &&
+           (n == 0 || wait(&ctl.dq_free, (n - 1) & 1, kStatusTimeoutMma));
+      if (!ok) break;
       tc_fence_after();
       issue_qk<D, ET>(tmem + C::kColDP, v_lo, do_lo);  // dP^T = V dO^T
       mma_commit_warp(&ctl.sd_full);
