@@ -419,7 +419,7 @@ def run_ours(args, w):
         "frac_of_peak": value / world / peak,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d * world,
                 "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms,
-                "api": "fmha_fwd_host, pinned host buffers, %s chunks" % (args.chunks or 8)},
+                "api": "fmha_fwd_host, pinned host buffers, %s chunks" % (args.chunks or 16)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_note,

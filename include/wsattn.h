@@ -105,18 +105,21 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
  *   dq, dk, dv, d_o, dlse
  *              caller-owned device staging buffers of the full sizes (same
  *              sizes and alignment rules as fmha_fwd's q, k, v, o, lse).
- *   n_chunks   0 for the default (8), else 1..64: the B*H (batch, head) slices
- *              are split into this many contiguous chunks.  The host-to-device
- *              copy of chunk c+1 and the device-to-host copy of chunk c-1 run on
- *              two copy streams while chunk c is computed on `stream`.
+ *   n_chunks   0 for the default (16), else 1..64: the B*H (batch, head)
+ *              slices are split into this many contiguous chunks.  The
+ *              host-to-device copy of chunk c+1 and the device-to-host copy of
+ *              chunk c-1 run on two copy streams while chunk c is computed.
+ *              Chunks alternate between `stream` and a second compute stream
+ *              of the library, so that a chunk's kernel can start on SMs the
+ *              previous chunk's last wave leaves idle.
  *   Other arguments as fmha_fwd.
  *
  * The rows of every (batch, head) slice are independent, so the result is
  * bit-identical to fmha_fwd on the staged device tensors.  The call returns
  * once all work is enqueued; every copy and kernel is complete when `stream`
- * is (synchronise `stream` before reading o and lse).  The two copy streams and
- * a few events are created once per device and host thread and reused; no
- * memory is allocated.  Errors as fmha_fwd (a bad pointer or size is
+ * is (synchronise `stream` before reading o and lse).  The library's three
+ * streams and a few events are created once per device and host thread and
+ * reused; no memory is allocated.  Errors as fmha_fwd (a bad pointer or size is
  * FMHA_ERR_INVALID_ARG before anything is enqueued).
  */
 fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,

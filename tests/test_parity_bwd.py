@@ -128,6 +128,30 @@ def test_bwd_bench_shape_sampled_slices():
         _compare("%s slice %d" % (w.describe(), bh), (dq[b, h], dk[b, h], dv[b, h]), ref, bound)
 
 
+def test_bwd_headline_shape_one_slice():
+    """The backward benchmark's default shape (B4 H32 S16384 D128 f16, the
+    launch bench.py times): every output finite, the last (batch, head) slice
+    compared in full to the oracle (an S x S problem, a few seconds of fp64
+    work on the host)."""
+    w = synthetic.by_name("b4h32s16k_d128_f16")
+    q, k, v = synthetic.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    do = torch.randn(q.shape, generator=g).to(q.dtype)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = wsa.attention(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = (torch.full_like(qd, float("nan")) for _ in range(3))
+    wsa.fmha_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, causal=w.causal, scale=w.scale)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all().item()
+    b, h = w.B - 1, w.H - 1
+    args = [t[b, h].double().numpy() for t in (q, k, v, do)]
+    got = [t[b, h].cpu().double().numpy() for t in (dq, dk, dv)]
+    ref, bound = _bounds(*args, o[b, h].cpu().double().numpy(), lse[b, h].cpu().double().numpy(),
+                         w.causal, w.scale, _u(w.dtype))
+    _compare("%s slice (%d, %d)" % (w.describe(), b, h), got, ref, bound)
+
+
 def test_bwd_rejects_e4m3_and_small_workspace():
     q = torch.zeros(1, 1, 128, 128, dtype=torch.float16, device="cuda")
     o, lse = wsa.attention(q, q, q)

@@ -291,12 +291,13 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   return FMHA_OK;
 }
 
-// Per host thread and device: the two copy streams and the events that chain
-// chunks between them and the caller's stream (created on first use).
+// Per host thread and device: the two copy streams, a second compute stream
+// and the events that chain chunks between them and the caller's stream
+// (created on first use).
 constexpr int kMaxChunks = 64;
 struct HostPipe {
   bool ready = false;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp = nullptr;
   cudaEvent_t copied[kMaxChunks], computed[kMaxChunks], entry = nullptr, done = nullptr;
 };
 thread_local HostPipe t_pipe[kMaxDevices];
@@ -311,6 +312,7 @@ fmha_status host_pipe(HostPipe** out) {
     const unsigned ev_flags = cudaEventDisableTiming;
     if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.comp, cudaStreamNonBlocking)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&hp.entry, ev_flags)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&hp.done, ev_flags)) != cudaSuccess)
       return cuda_fail(e, "copy stream/event creation");
@@ -343,22 +345,28 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
       overlaps(v, in_host, o, o_host) ||
       overlaps(lse, static_cast<size_t>(BH) * lslice, o, o_host))
     return FMHA_ERR_INVALID_ARG;
-  const int64_t chunks = std::min<int64_t>(n_chunks == 0 ? 8 : n_chunks, BH);
+  const int64_t chunks = std::min<int64_t>(n_chunks == 0 ? 16 : n_chunks, BH);
 
   HostPipe* hp = nullptr;
   const fmha_status ps = host_pipe(&hp);
   if (ps != FMHA_OK) return ps;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  // the copy streams start after everything already queued on `stream`
+  // the copy streams and the second compute stream start after everything
+  // already queued on `stream`
   if ((e = cudaEventRecord(hp->entry, st)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(hp->h2d, hp->entry, 0)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(hp->d2h, hp->entry, 0)) != cudaSuccess)
+      (e = cudaStreamWaitEvent(hp->d2h, hp->entry, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->comp, hp->entry, 0)) != cudaSuccess)
     return cuda_fail(e, "stream ordering");
   auto at = [](const void* p, size_t off) {
     return static_cast<void*>(static_cast<char*>(const_cast<void*>(p)) + off);
   };
   for (int64_t c = 0; c < chunks; ++c) {
+    // chunks alternate between two compute streams, so that one chunk's
+    // kernel can start on the SMs that the previous one's last wave leaves
+    // idle
+    cudaStream_t cs = (c & 1) ? hp->comp : st;
     const int64_t s0 = BH * c / chunks, s1 = BH * (c + 1) / chunks, n = s1 - s0;
     const size_t off = static_cast<size_t>(s0) * slice, bytes = static_cast<size_t>(n) * slice;
     const size_t ooff = static_cast<size_t>(s0) * oslice, obytes = static_cast<size_t>(n) * oslice;
@@ -370,15 +378,15 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
         (e = cudaMemcpyAsync(at(dv, off), at(v, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
             cudaSuccess ||
         (e = cudaEventRecord(hp->copied[c], hp->h2d)) != cudaSuccess ||
-        (e = cudaStreamWaitEvent(st, hp->copied[c], 0)) != cudaSuccess)
+        (e = cudaStreamWaitEvent(cs, hp->copied[c], 0)) != cudaSuccess)
       return cuda_fail(e, "host-to-device copy");
     // one (batch, head) range is a B = 1, H = n problem at offset pointers
     const fmha_status ks =
         fwd_impl(at(dq, off), at(dk, off), at(dv, off), at(d_o, ooff),
-                 static_cast<float*>(at(dlse, loff)), 1, n, S, D, causal, scale, dtype, stream, 0,
+                 static_cast<float*>(at(dlse, loff)), 1, n, S, D, causal, scale, dtype, cs, 0,
                  kDefaultWaitLimitNs);
     if (ks != FMHA_OK) return ks;
-    if ((e = cudaEventRecord(hp->computed[c], st)) != cudaSuccess ||
+    if ((e = cudaEventRecord(hp->computed[c], cs)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess ||
         (e = cudaMemcpyAsync(at(o, ooff), at(d_o, ooff), obytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
             cudaSuccess ||
@@ -386,7 +394,8 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
                              hp->d2h)) != cudaSuccess)
       return cuda_fail(e, "device-to-host copy");
   }
-  // `stream` completes after the last copy back
+  // `stream` completes after the last copy back, which follows every chunk's
+  // kernel on either compute stream
   if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(st, hp->done, 0)) != cudaSuccess)
     return cuda_fail(e, "stream ordering");
