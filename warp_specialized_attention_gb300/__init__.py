@@ -1,7 +1,8 @@
-"""GB300 (sm_103a) fused attention forward: O = softmax(scale * Q K^T [+ causal
-mask]) V and the per-row natural log-sum-exp, as the three-stage T/C/U loop of
-"Tawa: Automatic Warp Specialization for Modern GPUs with Asynchronous
-References", Section III-D, Algorithm 1, on one GPU.
+"""GB300 (sm_103a) fused attention: the forward O = softmax(scale * Q K^T
+[+ causal mask]) V with the per-row natural log-sum-exp, as the three-stage
+T/C/U loop of "Tawa: Automatic Warp Specialization for Modern GPUs with
+Asynchronous References", Section III-D, Algorithm 1; and its backward pass
+(dQ, dK, dV from the forward's O and LSE), on one GPU.
 
 This module is a thin ctypes binding of ``libwsattn.so`` (include/wsattn.h):
 it only checks tensor metadata and marshals pointers, sizes and the stream.
