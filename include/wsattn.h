@@ -193,6 +193,50 @@ fmha_status fmha_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              fmha_dtype dtype, void* stream);
 
 /*
+ * fmha_bwd_host_scratch_bytes -- bytes of device scratch fmha_bwd_host needs:
+ * staging for q, k, v, o, d_o, dq, dk, dv and lse plus fmha_bwd's workspace,
+ * each region starting on 256 bytes.  0 for non-positive sizes.
+ */
+size_t fmha_bwd_host_scratch_bytes(int64_t B, int64_t H, int64_t S, int64_t D);
+
+/*
+ * fmha_bwd_host -- fmha_bwd on host-resident tensors, with the host<->device
+ * transfers overlapped with the computation (the backward counterpart of
+ * fmha_fwd_host; the pages have none).
+ *
+ *   q, k, v, o, lse, d_o
+ *              host pointers, inputs in fmha_bwd's layouts (16-bit only).
+ *              Page-locked (pinned) memory lets the copies run asynchronously
+ *              and overlap; pageable memory works but serialises them.
+ *   dq, dk, dv host pointers, outputs in the same layout.
+ *   scratch, scratch_bytes
+ *              caller-owned device memory of at least
+ *              fmha_bwd_host_scratch_bytes() bytes, 256-byte aligned; its
+ *              contents need not be initialised and are overwritten.
+ *   n_chunks   0 for the default (16), else 1..64: the B*H (batch, head)
+ *              slices are split into this many contiguous chunks; each
+ *              chunk's inputs are copied in, its backward pass (delta, the
+ *              main kernel, the dQ conversion) runs, and its gradients are
+ *              copied back, with the copies on two library streams and the
+ *              chunks' work alternating between `stream` and a second
+ *              compute stream of the library.
+ *   Other arguments as fmha_bwd.
+ *
+ * Slices are independent, so dK and dV are bit-identical to fmha_bwd on the
+ * staged tensors; dQ sums its key blocks' parts in an unspecified order (as
+ * in fmha_bwd).  The call returns once all work is enqueued; everything is
+ * complete when `stream` is.  Streams and events are those of
+ * fmha_fwd_host; no memory is allocated.  Errors as fmha_bwd (a bad pointer
+ * or size, or too little scratch, is FMHA_ERR_INVALID_ARG before anything is
+ * enqueued).
+ */
+fmha_status fmha_bwd_host(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                          void* scratch, size_t scratch_bytes, int64_t B, int64_t H, int64_t S,
+                          int64_t D, int causal, float scale, fmha_dtype dtype, int n_chunks,
+                          void* stream);
+
+/*
  * fmha_get_device_status -- synchronise `stream`, then report and clear the
  * device status word of the current device.  Returns FMHA_ERR_TIMEOUT if any
  * kernel since the previous call abandoned a wait, FMHA_ERR_CUDA if the stream

@@ -195,3 +195,45 @@ def test_no_multicast_or_trap_in_sources():
         text = open(os.path.join(csrc, f)).read()
         for b in banned:
             assert b not in text, "%s uses %s" % (f, b)
+
+
+def test_backward_host_entry_validates_before_any_cuda_call(lib):
+    host = [_BASE + (10 + i) * (1 << 30) for i in range(9)]   # q k v o lse d_o dq dk dv
+    scratch = _BASE + 30 * (1 << 30)
+    need = lib.fmha_bwd_host_scratch_bytes(1, 2, 128, 128)
+
+    def call(h=host, sc=scratch, nbytes=need, S=128, n_chunks=0, dtype=0):
+        return lib.fmha_bwd_host(*h, sc, nbytes, 1, 2, S, 128, 0, 0.088, dtype, n_chunks, None)
+    for i in range(9):
+        bad = list(host)
+        bad[i] = 0
+        assert call(h=bad) == wsa.FMHA_ERR_INVALID_ARG
+    bad = list(host)
+    bad[4] += 2  # host lse must be 4-byte aligned
+    assert call(h=bad) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(sc=0) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(sc=scratch + 16) == wsa.FMHA_ERR_INVALID_ARG   # scratch: 256-byte aligned
+    assert call(nbytes=need - 1) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(n_chunks=-1) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(n_chunks=65) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(S=0) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(dtype=wsa.FMHA_E4M3) == wsa.FMHA_ERR_UNSUPPORTED
+    overl = list(host)
+    overl[6] = overl[0] + 64  # host dq overlapping host q
+    assert call(h=overl) == wsa.FMHA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():   # valid: the first CUDA call (stream creation) fails
+        assert call() == wsa.FMHA_ERR_CUDA
+
+
+def test_backward_host_scratch_size(lib):
+    """Eight (B*H*S*D) 16-bit staging tensors and the (B*H*S) float32 lse, each
+    rounded up to 256 bytes, then the workspace of fmha_bwd (B*H*S*(D + 1)
+    float32)."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    for B, H, S, D in ((1, 1, 17, 64), (2, 3, 1000, 128), (4, 32, 16384, 128)):
+        rows = B * H * S
+        want = 8 * up(rows * D * 2) + up(rows * 4) + rows * (D + 1) * 4
+        assert lib.fmha_bwd_host_scratch_bytes(B, H, S, D) == want
+    assert lib.fmha_bwd_host_scratch_bytes(1, 1, 17, 64) == 23108
+    assert lib.fmha_bwd_host_scratch_bytes(0, 1, 128, 64) == 0

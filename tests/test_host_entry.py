@@ -47,3 +47,38 @@ def test_host_entry_pageable_memory_and_reuse():
         wsa.fmha_fwd_host(q, k, v, o, lse, *staging, dl, scale=w.scale, n_chunks=3)
         torch.cuda.synchronize()
         assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, l_ref.cpu())
+
+
+@pytest.mark.parametrize("shape,causal,dtype,chunks", [
+    ((2, 3, 384, 128), False, torch.float16, 0),
+    ((2, 3, 384, 128), True, torch.bfloat16, 4),
+    ((1, 5, 300, 64), True, torch.float16, 1),
+    ((1, 2, 257, 64), False, torch.bfloat16, 64),   # more chunks than slices, ragged S
+])
+def test_bwd_host_entry_matches_device_entry(shape, causal, dtype, chunks):
+    """fmha_bwd_host against fmha_bwd on the same inputs.  A key block's dK and
+    dV are summed in TMEM in a fixed order, so they are bit-identical.  dQ adds
+    the key blocks' fp32 parts in an unspecified order, so the two may differ
+    by the rounding of that order: one unit in the last place of the 16-bit
+    result, plus fp32 cancellation noise near zero."""
+    B, H, S, D = shape
+    w = synthetic.Workload("bhost", B, H, S, D, "f16" if dtype == torch.float16 else "bf16",
+                           causal, 1.0, 321 + S)
+    q, k, v = synthetic.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    d_o = torch.randn(q.shape, generator=g).to(q.dtype)
+    o, lse = wsa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale)
+    ref = wsa.attention_backward(q.cuda(), k.cuda(), v.cuda(), o, lse, d_o.cuda(), causal=causal,
+                                 scale=w.scale)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    hin = [t.cpu().pin_memory() for t in (q, k, v, o, lse, d_o)]
+    hout = [torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory() for _ in range(3)]
+    wsa.fmha_bwd_host(*hin, *hout, causal=causal, scale=w.scale, n_chunks=chunks)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    dq_h, dk_h, dv_h = hout
+    dq_r, dk_r, dv_r = (t.cpu() for t in ref)
+    assert torch.equal(dk_h, dk_r) and torch.equal(dv_h, dv_r)
+    ulp = 2.0 ** -10 if dtype == torch.float16 else 2.0 ** -7
+    diff = (dq_h.float() - dq_r.float()).abs()
+    lim = ulp * dq_r.float().abs() + 1e-5 * float(dq_r.float().abs().max())
+    assert bool((diff <= lim).all()), "dQ differs by %.3e" % float(diff.max())

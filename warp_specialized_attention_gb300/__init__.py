@@ -26,7 +26,8 @@ __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
     "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
-    "fmha_bwd", "fmha_bwd_workspace_bytes", "fmha_bwd_noalloc", "attention_backward",
+    "fmha_bwd", "fmha_bwd_workspace_bytes", "fmha_bwd_noalloc", "fmha_bwd_host",
+    "fmha_bwd_host_scratch_bytes", "attention_backward",
     "get_device_status", "status_str", "version",
 ]
 
@@ -85,6 +86,12 @@ def load_library():
         lib.fmha_bwd_noalloc.argtypes = [vp] * 9 + [i64, i64, i64, i64, ctypes.c_int,
                                                     ctypes.c_float, ctypes.c_int, vp]
         lib.fmha_bwd_noalloc.restype = ctypes.c_int
+        lib.fmha_bwd_host_scratch_bytes.argtypes = [i64, i64, i64, i64]
+        lib.fmha_bwd_host_scratch_bytes.restype = ctypes.c_size_t
+        lib.fmha_bwd_host.argtypes = [vp] * 10 + [ctypes.c_size_t, i64, i64, i64, i64,
+                                                  ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                                  ctypes.c_int, vp]
+        lib.fmha_bwd_host.restype = ctypes.c_int
         lib.fmha_get_device_status.argtypes = [vp]
         lib.fmha_get_device_status.restype = ctypes.c_int
         lib.fmha_status_str.argtypes = [ctypes.c_int]
@@ -291,6 +298,54 @@ def fmha_bwd_noalloc(q, k, v, o, lse, d_o, dq, dk, dv, causal: bool = False,
                                   _dtype_code(q), _stream_handle(stream))
     if st != FMHA_OK:
         raise FmhaError(st, "fmha_bwd_noalloc", lib.fmha_last_cuda_error().decode())
+
+
+def fmha_bwd_host_scratch_bytes(B: int, H: int, S: int, D: int) -> int:
+    """Bytes of device scratch fmha_bwd_host needs (C ABI
+    fmha_bwd_host_scratch_bytes)."""
+    return int(load_library().fmha_bwd_host_scratch_bytes(B, H, S, D))
+
+
+def fmha_bwd_host(q, k, v, o, lse, d_o, dq, dk, dv, scratch=None, causal: bool = False,
+                  scale: float | None = None, n_chunks: int = 0, stream=None,
+                  device=None) -> None:
+    """Enqueue the backward pass on host tensors with overlapped transfers (C
+    ABI fmha_bwd_host): q, k, v, o, d_o (B, H, S, D) 16-bit and lse (B, H, S)
+    float32 are CPU inputs, dq, dk, dv CPU outputs of q's shape and dtype
+    (pinned for overlap).  ``scratch`` is a CUDA uint8 tensor of at least
+    fmha_bwd_host_scratch_bytes(B, H, S, D) bytes; one is allocated with torch
+    on ``device`` (default: the current device) when it is None.  Synchronise
+    ``stream`` before reading dq, dk, dv."""
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("d_o", d_o), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CPU tensor" % name)
+        if t.dim() != 4 or t.shape != q.shape or t.dtype != q.dtype:
+            raise ValueError("%s must match q's (B, H, S, D) shape and dtype" % name)
+    if q.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("fmha_bwd_host takes float16 or bfloat16 tensors")
+    B, H, S, D = q.shape
+    if (not isinstance(lse, torch.Tensor) or lse.is_cuda or not lse.is_contiguous()
+            or lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S)):
+        raise ValueError("lse must be a contiguous CPU float32 tensor of shape (B, H, S)")
+    need = fmha_bwd_host_scratch_bytes(B, H, S, D)
+    if scratch is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+    if not scratch.is_cuda or scratch.numel() * scratch.element_size() < need:
+        raise ValueError("scratch must be a CUDA tensor of at least %d bytes" % need)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(scratch.device):
+        st = lib.fmha_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), d_o.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), scratch.data_ptr(),
+                               scratch.numel() * scratch.element_size(), B, H, S, D,
+                               int(bool(causal)), float(scale), _dtype_code(q), int(n_chunks),
+                               _stream_handle(stream))
+    if st != FMHA_OK:
+        raise FmhaError(st, "fmha_bwd_host", lib.fmha_last_cuda_error().decode())
 
 
 def attention_backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None,

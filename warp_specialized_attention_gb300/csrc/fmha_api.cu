@@ -134,13 +134,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-fmha_status validate(const void* q, const void* k, const void* v, void* o, float* lse,
-                     int64_t B, int64_t H, int64_t S, int64_t D, float scale, int dtype) {
-  if (!q || !k || !v || !o || !lse) return FMHA_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
-    return FMHA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
+// Sizes, scale and element type (no pointer).
+fmha_status validate_sizes(int64_t B, int64_t H, int64_t S, int64_t D, float scale, int dtype) {
   if (B < 1 || H < 1 || S < 1 || D < 1) return FMHA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FMHA_ERR_INVALID_ARG;
   if (dtype != FMHA_F16 && dtype != FMHA_BF16 && dtype != FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
@@ -150,6 +145,18 @@ fmha_status validate(const void* q, const void* k, const void* v, void* o, float
   if (B > lim || H > lim || S > lim || B * H > lim) return FMHA_ERR_INVALID_ARG;
   const int64_t nq = (S + 255) / 256;
   if (nq * B * H > lim) return FMHA_ERR_INVALID_ARG;
+  return FMHA_OK;
+}
+
+fmha_status validate(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t S, int64_t D, float scale, int dtype) {
+  if (!q || !k || !v || !o || !lse) return FMHA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o)) & 15u)
+    return FMHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
+  const fmha_status vs = validate_sizes(B, H, S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
   const size_t n = static_cast<size_t>(B * H) * static_cast<size_t>(S) * static_cast<size_t>(D);
   const size_t ib = n * in_bytes(dtype), ob = n * kOutBytes;
   const size_t lb = static_cast<size_t>(B * H * S) * 4;
@@ -217,11 +224,11 @@ size_t bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
   return rows * static_cast<size_t>(D) * 4 + rows * 4;  // dQ accumulator + delta, fp32
 }
 
-fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
-                     const float* lse, const void* d_o, void* dq, void* dk, void* dv,
-                     void* workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t S,
-                     int64_t D, int causal, float scale, int dtype, void* stream,
-                     uint64_t wait_limit_ns) {
+// Argument checks of the backward pass (no CUDA call).
+fmha_status bwd_validate(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t S,
+                         int64_t D, float scale, int dtype) {
   if (dtype == FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
   // q, k, v, o, lse as in the forward (o is an input here)
   const fmha_status vs = validate(q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, H,
@@ -247,7 +254,17 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
     for (int j = 0; j < i; ++j)
       if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j])) return FMHA_ERR_INVALID_ARG;
   }
+  return FMHA_OK;
+}
 
+// Enqueues the backward pass of BH (batch, head) slices on `st`: clear the
+// dQ accumulator, delta, the main kernel, the dQ conversion.  The arguments
+// have been checked; dq_acc holds BH*S*D and delta BH*S floats.
+fmha_status bwd_enqueue(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                        float* dq_acc, float* delta, int64_t BH, int64_t S, int64_t D, int causal,
+                        float scale, int dtype, cudaStream_t st, uint64_t wait_limit_ns) {
+  const int64_t n_blk = (S + 127) / 128;
   cudaError_t e;
   EncodeTiledFn enc = encode_fn(&e);
   if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
@@ -259,10 +276,7 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if ((e = status_word(&status)) != cudaSuccess)
     return cuda_fail(e, "cudaGetSymbolAddress(status)");
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool bf16 = dtype == FMHA_BF16;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = dq_acc + static_cast<size_t>(BH * S * D);
   alignas(64) CUtensorMap tdq;
   if (!encode_dq_map(enc, &tdq, dq_acc, BH, S, D))
     return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(dQ accumulator)");
@@ -289,6 +303,21 @@ fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if ((e = wsa::launch_bwd_dq(bf16, dq_acc, dq, BH * S * D, st)) != cudaSuccess)
     return cuda_fail(e, "dQ conversion launch");
   return FMHA_OK;
+}
+
+fmha_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, int64_t B, int64_t H, int64_t S,
+                     int64_t D, int causal, float scale, int dtype, void* stream,
+                     uint64_t wait_limit_ns) {
+  const fmha_status vs = bwd_validate(q, k, v, o, lse, d_o, dq, dk, dv, workspace,
+                                      workspace_bytes, B, H, S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
+  const int64_t BH = B * H;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = dq_acc + static_cast<size_t>(BH * S * D);
+  return bwd_enqueue(q, k, v, o, lse, d_o, dq, dk, dv, dq_acc, delta, BH, S, D, causal, scale,
+                     dtype, static_cast<cudaStream_t>(stream), wait_limit_ns);
 }
 
 // Per host thread and device: the two copy streams, a second compute stream
@@ -402,6 +431,125 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
   return FMHA_OK;
 }
 
+// Device scratch of fmha_bwd_host: staged q, k, v, o, d_o, dq, dk, dv, then
+// lse, then the backward workspace; every region starts on 256 bytes.
+struct BwdHostLayout {
+  size_t q, k, v, o, d_o, dq, dk, dv, lse, ws, ws_bytes, total;
+};
+
+BwdHostLayout bwd_host_layout(int64_t B, int64_t H, int64_t S, int64_t D) {
+  auto up = [](size_t x) { return (x + 255) & ~size_t{255}; };
+  const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(S);
+  const size_t tb = up(rows * static_cast<size_t>(D) * 2), lb = up(rows * 4);
+  BwdHostLayout L;
+  size_t off = 0;
+  size_t* tensors[8] = {&L.q, &L.k, &L.v, &L.o, &L.d_o, &L.dq, &L.dk, &L.dv};
+  for (size_t* t : tensors) {
+    *t = off;
+    off += tb;
+  }
+  L.lse = off;
+  off += lb;
+  L.ws = off;
+  L.ws_bytes = bwd_workspace_bytes(B, H, S, D);
+  L.total = off + L.ws_bytes;
+  return L;
+}
+
+fmha_status bwd_host_impl(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                          void* scratch, size_t scratch_bytes, int64_t B, int64_t H, int64_t S,
+                          int64_t D, int causal, float scale, int dtype, int n_chunks,
+                          void* stream) {
+  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !scratch)
+    return FMHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(scratch) & 255u) return FMHA_ERR_INVALID_ARG;
+  if (n_chunks < 0 || n_chunks > kMaxChunks) return FMHA_ERR_INVALID_ARG;
+  if (dtype == FMHA_E4M3) return FMHA_ERR_UNSUPPORTED;
+  // sizes first, then the layout that depends on them
+  const fmha_status sz = validate_sizes(B, H, S, D, scale, dtype);
+  if (sz != FMHA_OK) return sz;
+  const BwdHostLayout L = bwd_host_layout(B, H, S, D);
+  if (scratch_bytes < L.total) return FMHA_ERR_INVALID_ARG;
+  char* base = static_cast<char*>(scratch);
+  const fmha_status vs = bwd_validate(base + L.q, base + L.k, base + L.v, base + L.o,
+                                      reinterpret_cast<float*>(base + L.lse), base + L.d_o,
+                                      base + L.dq, base + L.dk, base + L.dv, base + L.ws,
+                                      L.ws_bytes, B, H, S, D, scale, dtype);
+  if (vs != FMHA_OK) return vs;
+  const int64_t BH = B * H;
+  // host side: outputs may not overlap the inputs or one another
+  const size_t tb = static_cast<size_t>(BH * S * D) * 2, lb = static_cast<size_t>(BH * S) * 4;
+  const void* ins[6] = {q, k, v, o, d_o, lse};
+  const size_t in_sz[6] = {tb, tb, tb, tb, tb, lb};
+  void* outs[3] = {dq, dk, dv};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(outs[i], tb, ins[j], in_sz[j])) return FMHA_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (overlaps(outs[i], tb, outs[j], tb)) return FMHA_ERR_INVALID_ARG;
+  }
+  const int64_t chunks = std::min<int64_t>(n_chunks == 0 ? 16 : n_chunks, BH);
+
+  HostPipe* hp = nullptr;
+  const fmha_status ps = host_pipe(&hp);
+  if (ps != FMHA_OK) return ps;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaEventRecord(hp->entry, st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->h2d, hp->entry, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->d2h, hp->entry, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->comp, hp->entry, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  auto at = [](const void* p, size_t off) {
+    return static_cast<void*>(static_cast<char*>(const_cast<void*>(p)) + off);
+  };
+  const size_t slice = static_cast<size_t>(S * D) * 2, lslice = static_cast<size_t>(S) * 4;
+  float* dq_acc_all = reinterpret_cast<float*>(base + L.ws);
+  float* delta_all = dq_acc_all + static_cast<size_t>(BH * S * D);
+  const void* host_in[5] = {q, k, v, o, d_o};
+  const size_t dev_in[5] = {L.q, L.k, L.v, L.o, L.d_o};
+  void* host_out[3] = {dq, dk, dv};
+  const size_t dev_out[3] = {L.dq, L.dk, L.dv};
+  for (int64_t c = 0; c < chunks; ++c) {
+    // chunks alternate between two compute streams (see fwd_host_impl)
+    cudaStream_t cs = (c & 1) ? hp->comp : st;
+    const int64_t s0 = BH * c / chunks, s1 = BH * (c + 1) / chunks, n = s1 - s0;
+    const size_t off = static_cast<size_t>(s0) * slice, bytes = static_cast<size_t>(n) * slice;
+    const size_t loff = static_cast<size_t>(s0) * lslice, lbytes = static_cast<size_t>(n) * lslice;
+    for (int i = 0; i < 5; ++i)
+      if ((e = cudaMemcpyAsync(base + dev_in[i] + off, at(host_in[i], off), bytes,
+                               cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    if ((e = cudaMemcpyAsync(base + L.lse + loff, at(lse, loff), lbytes, cudaMemcpyHostToDevice,
+                             hp->h2d)) != cudaSuccess ||
+        (e = cudaEventRecord(hp->copied[c], hp->h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(cs, hp->copied[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "host-to-device copy");
+    // slices [s0, s1) are a B = 1, H = n problem at offset pointers, with
+    // their own part of the dQ accumulator and of delta
+    const fmha_status ks = bwd_enqueue(
+        base + L.q + off, base + L.k + off, base + L.v + off, base + L.o + off,
+        reinterpret_cast<const float*>(base + L.lse + loff), base + L.d_o + off,
+        base + L.dq + off, base + L.dk + off, base + L.dv + off,
+        dq_acc_all + static_cast<size_t>(s0 * S * D), delta_all + static_cast<size_t>(s0 * S), n,
+        S, D, causal, scale, dtype, cs, kDefaultWaitLimitNs);
+    if (ks != FMHA_OK) return ks;
+    if ((e = cudaEventRecord(hp->computed[c], cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "stream ordering");
+    for (int i = 0; i < 3; ++i)
+      if ((e = cudaMemcpyAsync(at(host_out[i], off), base + dev_out[i] + off, bytes,
+                               cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+  }
+  if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(st, hp->done, 0)) != cudaSuccess)
+    return cuda_fail(e, "stream ordering");
+  return FMHA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -430,6 +578,20 @@ fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, 
                           fmha_dtype dtype, int n_chunks, void* stream) {
   return fwd_host_impl(q, k, v, o, lse, dq, dk, dv, d_o, dlse, B, H, S, D, causal, scale,
                        static_cast<int>(dtype), n_chunks, stream);
+}
+
+size_t fmha_bwd_host_scratch_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
+  if (B < 1 || H < 1 || S < 1 || D < 1) return 0;
+  return bwd_host_layout(B, H, S, D).total;
+}
+
+fmha_status fmha_bwd_host(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* d_o, void* dq, void* dk, void* dv,
+                          void* scratch, size_t scratch_bytes, int64_t B, int64_t H, int64_t S,
+                          int64_t D, int causal, float scale, fmha_dtype dtype, int n_chunks,
+                          void* stream) {
+  return bwd_host_impl(q, k, v, o, lse, d_o, dq, dk, dv, scratch, scratch_bytes, B, H, S, D,
+                       causal, scale, static_cast<int>(dtype), n_chunks, stream);
 }
 
 size_t fmha_bwd_workspace_bytes(int64_t B, int64_t H, int64_t S, int64_t D) {
