@@ -5,7 +5,8 @@
 // five products per 128-row query block.  Three of them have forward forms:
 //   S^T  = K Q^T      (issue_qk: both operands K-major)
 //   dP^T = V dO^T     (issue_qk)
-//   dV  += P^T dO     (issue_pv: P^T from TMEM, dO MN-major)
+//   dV  += P^T dO     (issue_dv: the forward's P V form, with P^T from TMEM in
+//                     two 32-column groups, dO MN-major)
 // The other two take their A operand from one shared-memory tile of dS^T
 // (128 keys x 128 queries, 16-bit, two 64-column blocks, 128-byte swizzle):
 //   dK  += dS^T Q     A = dS^T read K-major (keys = M, queries = K),
