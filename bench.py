@@ -39,6 +39,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import shutil
 import statistics
 import subprocess
@@ -116,11 +117,19 @@ def _peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
 
 
+def _code_only(text):
+    """C/C++/CUDA source without comments and blank lines: a comment edit does
+    not change the compiled kernel, so it keeps its recorded counters."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def _kernel_sha(sources=None):
     h = hashlib.sha256()
     for f in (KERNEL_SOURCES if sources is None else sources):
-        with open(os.path.join(ROOT, "warp_specialized_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "warp_specialized_attention_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
