@@ -152,6 +152,24 @@ def test_bwd_headline_shape_one_slice():
     _compare("%s slice (%d, %d)" % (w.describe(), b, h), got, ref, bound)
 
 
+def test_bwd_d64_sharp_causal_shape_sampled_slices():
+    """B2 H16 S8192 D64 f16 causal with K scaled by 4 (logits spread four
+    times wider, a sharply peaked softmax): every output finite, the first and
+    last (batch, head) slices compared in full to the oracle."""
+    w = synthetic.by_name("b2h16s8k_d64_f16_causal_ksharp")
+    q, k, v = synthetic.make_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + 1)
+    do = torch.randn(q.shape, generator=g).to(q.dtype)
+    o, lse, dq, dk, dv = _run_gpu(q, k, v, do, w.causal, w.scale)
+    for t in (dq, dk, dv):
+        assert np.isfinite(t).all()
+    for bh in (0, w.B * w.H - 1):
+        b, h = divmod(bh, w.H)
+        args = [t[b, h].double().numpy() for t in (q, k, v, do)]
+        ref, bound = _bounds(*args, o[b, h], lse[b, h], w.causal, w.scale, _u(w.dtype))
+        _compare("%s slice %d" % (w.describe(), bh), (dq[b, h], dk[b, h], dv[b, h]), ref, bound)
+
+
 def test_bwd_rejects_e4m3_and_small_workspace():
     q = torch.zeros(1, 1, 128, 128, dtype=torch.float16, device="cuda")
     o, lse = wsa.attention(q, q, q)
