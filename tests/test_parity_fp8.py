@@ -139,6 +139,22 @@ def test_e4m3_named_workload_sampled(w):
     _check(o, lse, q, k, v, picks, w.causal, w.scale, w.describe() + " (sampled rows)")
 
 
+def test_e4m3_causal_4k_sampled():
+    """E4M3 at B4 H32 S4096 causal: 2048 units handed out longest first in
+    head groups, so most blocks run a dozen units of different lengths;
+    sampled rows of three slices against the oracle, and no device-side
+    wait may give up."""
+    w = synthetic.Workload("e4m3-causal-4k", 4, 32, 4096, 128, "e4m3", True, 1.0, 7104)
+    q, k, v = synthetic.make_inputs(w)
+    o, lse = _gpu(q, k, v, w.causal, w.scale)
+    rng = np.random.default_rng(w.seed)
+    picks = []
+    for bh in (0, 64, 127):
+        rows = {0, 1, 127, 128, 255, 256, w.S - 1} | set(rng.integers(0, w.S, size=24).tolist())
+        picks.append((divmod(bh, w.H), np.array(sorted(rows), dtype=np.int64)))
+    _check(o, lse, q, k, v, picks, w.causal, w.scale, w.describe() + " (sampled rows)")
+
+
 def test_e4m3_threshold_knob():
     """The E4M3 threshold may be set anywhere in [0, 8] (P then stored as
     2^(8-tau) P; 8 is the default): the result must stay within the bounds."""
