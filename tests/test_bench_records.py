@@ -1,0 +1,35 @@
+"""bench.py's link between the committed DRAM counters and the kernel sources
+(CPU only): a record counts only while the kernel code it was taken on is
+unchanged; comments do not count as code."""
+import json
+import os
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_comments_and_blank_lines_do_not_change_the_code():
+    a = "int f(int x) {\n  return x + 1;  // add one\n}\n"
+    b = "/* a comment\n   over lines */\nint f(int x) {\n\n  return x + 1;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+
+
+def test_a_code_edit_changes_the_code():
+    a = "int f(int x) { return x + 1; }  // one\n"
+    b = "int f(int x) { return x + 2; }  // one\n"
+    assert bench._code_only(a) != bench._code_only(b)
+
+
+def test_every_traffic_record_matches_its_kernel_sources():
+    """The committed records were taken on the kernels as they are now; a
+    kernel change without a new capture shows up here (and as a null traffic
+    in the bench line)."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    assert records
+    for name, rec in records.items():
+        sources = bench.BWD_SOURCES if name.endswith("_bwd") else None
+        assert rec["kernel_sha"] == bench._kernel_sha(sources), name
+        assert rec["bytes_per_launch"] > 0
+        assert os.path.exists(os.path.join(ROOT, rec["source"].split(" ")[0].split(":")[0]))
