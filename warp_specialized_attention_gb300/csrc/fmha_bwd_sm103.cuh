@@ -108,7 +108,8 @@ struct BwdCfg {
   static constexpr int kOffStat = kOffDQ + kBwdDqWarps * kDqStage;  // 2 x (LSE*log2e, delta)
   static constexpr int kOffCtl = kOffStat + 2 * 256 * 4;
   static constexpr int kSmemBytes = 1024 + kOffCtl + 256;
-  // TMEM columns: S^T (P^T over its first 64), dP^T (dQ reuses it), dV, dK
+  // TMEM columns: S^T (16-bit P^T over columns 0-31 and 64-95 of it), dP^T
+  // (dQ reuses it), dV, dK
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128;
   static constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 };
