@@ -53,8 +53,10 @@
 // must rescale O_t mid-block), o_full[t] (commit after the last P_t V).
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
-// O_1 [256+D,256+2D).  P_t (16-bit, two per column) overwrites the first 64
-// columns of S_t once the softmax has read S_t into registers.
+// O_1 [256+D,256+2D).  At D = 128, P_t overwrites the first columns of S_t
+// once the softmax has read S_t into registers: 64 columns of 16-bit P (two
+// per column) or 32 of E4M3 P (four per column).  At D = 64, P_t has columns
+// of its own after the O tiles (split P, below).
 //
 // Online softmax with a lazy maximum: the running maximum m (in log2 units of
 // the scaled logits) is only raised when a block's maximum exceeds it by more
