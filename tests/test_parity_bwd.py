@@ -177,3 +177,29 @@ def test_bwd_rejects_e4m3_and_small_workspace():
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(ValueError):
         wsa.fmha_bwd(q, q, q, o, lse, q, dq, dk, dv, workspace=small)
+
+
+@pytest.mark.parametrize("causal,dtype", [(False, torch.float16), (True, torch.bfloat16)])
+def test_autograd_wrapper_matches_the_entry_points(causal, dtype):
+    """flash_attention through torch.autograd gives the outputs of attention()
+    and the gradients of fmha_bwd for the incoming gradient (dK, dV bit for
+    bit; dQ sums its key blocks in an unspecified order, so to 16-bit
+    rounding); the entry points themselves are checked against the oracle
+    above."""
+    w = synthetic.Workload("autograd", 2, 3, 520, 64, "f16" if dtype == torch.float16 else "bf16",
+                           causal, 1.0, 4242)
+    q, k, v = (t.cuda() for t in synthetic.make_inputs(w))
+    g = torch.Generator().manual_seed(7)
+    d_o = torch.randn(q.shape, generator=g).to(dtype).cuda()
+    qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = wsa.flash_attention(qa, ka, va, causal=causal, scale=w.scale)
+    o.backward(d_o)
+    o_ref, lse_ref = wsa.attention(q, k, v, causal=causal, scale=w.scale)
+    dq_r, dk_r, dv_r = wsa.attention_backward(q, k, v, o_ref, lse_ref, d_o, causal=causal,
+                                              scale=w.scale)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    assert torch.equal(o.detach(), o_ref)
+    assert torch.equal(ka.grad, dk_r) and torch.equal(va.grad, dv_r)
+    ulp = 2.0 ** -10 if dtype == torch.float16 else 2.0 ** -7
+    diff = (qa.grad.float() - dq_r.float()).abs()
+    assert bool((diff <= ulp * dq_r.float().abs() + 1e-5 * float(dq_r.float().abs().max())).all())

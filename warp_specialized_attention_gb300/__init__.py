@@ -27,7 +27,8 @@ __all__ = [
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
     "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
     "fmha_bwd", "fmha_bwd_workspace_bytes", "fmha_bwd_noalloc", "fmha_bwd_host",
-    "fmha_bwd_host_scratch_bytes", "attention_backward",
+    "fmha_bwd_host_scratch_bytes", "attention_backward", "AttentionFunction",
+    "flash_attention",
     "get_device_status", "status_str", "version",
 ]
 
@@ -354,3 +355,35 @@ def attention_backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float 
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fmha_bwd(q, k, v, o, lse, d_o, dq, dk, dv, causal=causal, scale=scale, stream=stream)
     return dq, dk, dv
+
+
+class AttentionFunction(torch.autograd.Function):
+    """Differentiable attention on the library's kernels: the forward runs
+    fmha_fwd and keeps O and LSE, the backward runs fmha_bwd with them.
+    16-bit (float16 / bfloat16) tensors of shape (B, H, S, D), D 64 or 128;
+    E4M3 inputs are forward-only."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal=False, scale=None):
+        if scale is None:
+            scale = 1.0 / math.sqrt(q.shape[-1])
+        o, lse = attention(q, k, v, causal=causal, scale=scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale = bool(causal), float(scale)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, d_o, d_lse):
+        if d_lse is not None and bool(torch.any(d_lse != 0)):
+            raise NotImplementedError("gradients through the log-sum-exp output are not supported")
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attention_backward(q, k, v, o, lse, d_o.contiguous(), causal=ctx.causal,
+                                        scale=ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def flash_attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """O = softmax(scale * Q K^T [+ causal mask]) V, differentiable with respect
+    to q, k and v (AttentionFunction); returns O only."""
+    o, _ = AttentionFunction.apply(q, k, v, causal, scale)
+    return o
