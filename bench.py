@@ -319,12 +319,54 @@ def run_reference(args, w):
     return 0
 
 
-def _config(w):
+L2_BYTES = 129 * 10 ** 6  # GB300 L2
+
+
+def _config(w, in_bytes=None, flushed=None):
+    """The workload, and how the timed steps treat L2: inputs larger than L2
+    run back to back; inputs that fit are evicted between timed launches."""
+    if in_bytes is None:
+        in_bytes = 3 * w.B * w.H * w.S * w.D * (1 if w.dtype == "e4m3" else 2)
+    if flushed is None:
+        l2 = "inputs %.3f GB (timed on the host cores: no GPU L2)" % (in_bytes / 1e9)
+    elif flushed:
+        l2 = ("inputs %.3f GB fit in the 129 MB L2: %d MB written between timed launches, "
+              "outside their events" % (in_bytes / 1e9, 2 * L2_BYTES // 10 ** 6))
+    else:
+        l2 = "inputs %.2f GB > 129 MB L2: no flush between steps" % (in_bytes / 1e9)
     return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "dtype": w.dtype,
             "causal": w.causal, "k_mult": w.k_mult, "scale": w.scale,
-            "layout": "BHSD contiguous, LSE fp32 (B,H,S)",
-            "l2": "inputs %.2f GB > 129 MB L2: no flush between steps"
-                  % (3 * w.B * w.H * w.S * w.D * 2 / 1e9)}
+            "layout": "BHSD contiguous, LSE fp32 (B,H,S)", "l2": l2}
+
+
+def _timed_steps(step, n, stream, device, in_bytes):
+    """n calls of step() on `stream`, one CUDA event pair per call.  Inputs
+    larger than L2 run back to back and the total is first to last event.
+    Inputs that fit in L2 are evicted before every call by writing twice the
+    L2 size, outside the call's own events, and the total is the sum of the
+    calls' times.  Returns (per-call ms, total ms, whether L2 was flushed)."""
+    flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+             if in_bytes <= L2_BYTES else None)
+    if flush is None:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record(stream)
+        for i in range(n):
+            step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(device)
+        launches = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+        return launches, ev[0].elapsed_time(ev[-1]), False
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    launches = [starts[i].elapsed_time(ends[i]) for i in range(n)]
+    return launches, sum(launches), True
 
 
 def run_ours(args, w):
@@ -351,20 +393,16 @@ def run_ours(args, w):
         raise SystemExit("device status error after warm-up")
 
     # ---- device-resident timing: one event pair per launch, on the launch stream
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
     sampler = ClockSampler(device) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     _barrier(dist, device)
     torch.cuda.synchronize(device)
-    ev[0].record(stream)
-    for i in range(args.steps):
-        wsa.fmha_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale, stream=stream)
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(device)
+    launches, total_ms, flushed = _timed_steps(
+        lambda: wsa.fmha_fwd(q, k, v, o, lse, causal=w.causal, scale=w.scale, stream=stream),
+        args.steps, stream, device, in_bytes)
     _barrier(dist, device)
     clocks = sampler.stop() if sampler else None
-    launches = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = _max_over_ranks(dist, total_ms, device)
     if wsa.get_device_status(stream) != wsa.FMHA_OK:
         raise SystemExit("device status error in the timed region")
@@ -424,7 +462,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic", "config": _config(w),
+        "dtype": w.dtype, "data": "synthetic", "config": _config(w, in_bytes, flushed),
         "frac_of_peak": value / world / peak,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d * world,
                 "d2h_bytes_per_step": d2h * world, "ms_per_step": e2e_ms,
@@ -469,20 +507,15 @@ def run_ours_bwd(args, w):
     torch.cuda.synchronize(device)
     if wsa.get_device_status(stream) != wsa.FMHA_OK:
         raise SystemExit("device status error after warm-up")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, lse, d_o))
     sampler = ClockSampler(device) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     _barrier(dist, device)
     torch.cuda.synchronize(device)
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize(device)
+    launches, total_ms, flushed = _timed_steps(step, args.steps, stream, device, in_bytes)
     _barrier(dist, device)
     clocks = sampler.stop() if sampler else None
-    launches = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = _max_over_ranks(dist, ev[0].elapsed_time(ev[-1]), device)
+    total_ms = _max_over_ranks(dist, total_ms, device)
     if wsa.get_device_status(stream) != wsa.FMHA_OK:
         raise SystemExit("device status error in the timed region")
     flops = 2.5 * w.flops
@@ -538,7 +571,7 @@ def run_ours_bwd(args, w):
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(_config(w), **{"pass": "backward"}),
+        "config": dict(_config(w, in_bytes, flushed), **{"pass": "backward"}),
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
                 "ms_per_step": e2e_ms, "api": "fmha_bwd_host, pinned host buffers, %s chunks" % (args.chunks or 16)},
