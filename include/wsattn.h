@@ -87,7 +87,9 @@ typedef enum { FMHA_F16 = 0, FMHA_BF16 = 1, FMHA_E4M3 = 2 } fmha_dtype;
  * enqueued.  Otherwise one kernel is enqueued and the call returns without
  * waiting for it (FMHA_ERR_CUDA if the launch itself failed).  A device-side
  * timeout is reported by the next fmha_get_device_status().  Safe to call from
- * several host threads on different streams.
+ * several host threads on different streams; note that the timeout status is
+ * one word per device, shared by every stream and thread (see
+ * fmha_get_device_status).
  */
 fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
@@ -102,9 +104,11 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
  *              Page-locked (pinned) memory lets the copies run asynchronously
  *              and overlap; pageable memory works but serialises them.
  *   o, lse     host pointers, outputs in the same layouts as fmha_fwd.
- *   dq, dk, dv, d_o, dlse
- *              caller-owned device staging buffers of the full sizes (same
- *              sizes and alignment rules as fmha_fwd's q, k, v, o, lse).
+ *   q_dev, k_dev, v_dev, o_dev, lse_dev
+ *              caller-owned device staging buffers for q, k, v, o and lse, of
+ *              the full sizes (the sizes and alignment rules of fmha_fwd's q,
+ *              k, v, o, lse).  Their contents on entry do not matter; on
+ *              return they hold the staged inputs and the outputs.
  *   n_chunks   0 for the default (16), else 1..64: the B*H (batch, head)
  *              slices are split into this many contiguous chunks.  The
  *              host-to-device copy of chunk c+1 and the device-to-host copy of
@@ -123,8 +127,8 @@ fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float
  * FMHA_ERR_INVALID_ARG before anything is enqueued).
  */
 fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
-                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
-                          int64_t H, int64_t S, int64_t D, int causal, float scale,
+                          void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev,
+                          int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
                           fmha_dtype dtype, int n_chunks, void* stream);
 
 /*
@@ -172,8 +176,11 @@ fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o,
  * fmha_bwd_noalloc -- fmha_bwd without a workspace argument: the dQ
  * accumulator and delta live in a device array of the library (96 MiB, one
  * per device), so the call needs no memory from the caller or an allocator.
- * The pages have no counterpart; it serves callers that cannot provide
- * scratch (a fixed memory budget, or a graph captured once and replayed).
+ * The pages have no counterpart.  It serves callers that cannot hand the
+ * backward a workspace because they may not allocate device memory while
+ * they run: a runtime that reserves its whole device-memory budget up front
+ * and forbids later cudaMalloc calls, or code inside another library's
+ * allocation-free region.
  *
  *   Arguments as fmha_bwd, minus workspace and workspace_bytes.
  *   Capacity: B*H*S*(4*D + 4) bytes must fit in 96 MiB (B*H*S <= 195,084
@@ -183,8 +190,8 @@ fmha_status fmha_bwd(const void* q, const void* k, const void* v, const void* o,
  *   overlaps in time (different streams, or several host threads) corrupt
  *   each other's dQ; serialise them (one stream, or events).
  *   Set-up: the first call on a device looks up the array's address
- *   (cudaGetSymbolAddress); make that first call before any stream capture,
- *   and capture later calls freely.
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
  * Errors as fmha_bwd.
  */
 fmha_status fmha_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
@@ -241,6 +248,14 @@ fmha_status fmha_bwd_host(const void* q, const void* k, const void* v, const voi
  * device status word of the current device.  Returns FMHA_ERR_TIMEOUT if any
  * kernel since the previous call abandoned a wait, FMHA_ERR_CUDA if the stream
  * reported an error, FMHA_OK otherwise.
+ *
+ * Scope: the status word is one per device, shared by every stream and host
+ * thread that launches this library's kernels there.  The call waits only for
+ * `stream`: a timeout raised by a kernel still running on another stream is
+ * not seen yet, and a timeout raised on any stream is reported (and cleared)
+ * by whichever caller reads the word first.  Callers on several streams that
+ * need per-stream attribution synchronise the device (or every such stream)
+ * before this call, and read it from one thread.
  */
 fmha_status fmha_get_device_status(void* stream);
 

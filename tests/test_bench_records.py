@@ -34,3 +34,29 @@ def test_a_record_is_used_only_while_its_kernel_code_is_unchanged():
         got = bench._traffic(name, sources)
         assert got == (rec["bytes_per_launch"] if current else None), name
         assert os.path.exists(os.path.join(ROOT, rec["source"].split(" ")[0].split(":")[0]))
+
+
+def test_each_line_names_the_workload_it_measured():
+    """The headline forward keeps the benchmark's own metric name; every other
+    forward or backward line names its own shape, dtype and mask."""
+    import synthetic
+    assert bench.metric_for(synthetic.HEADLINE) == bench.METRIC
+    names = set()
+    for w in synthetic.WORKLOADS + synthetic.FP8_WORKLOADS:
+        for pass_ in ("fwd", "bwd"):
+            m = bench.metric_for(w, pass_)
+            names.add(m)
+            assert ("bwd" in m) == (pass_ == "bwd")
+            if not (w is synthetic.HEADLINE and pass_ == "fwd"):
+                assert w.describe() in m
+    assert len(names) == 2 * len(synthetic.WORKLOADS + synthetic.FP8_WORKLOADS)
+
+
+def test_default_run_covers_every_named_configuration():
+    """The default bench line carries, besides the headline, a record for each
+    of the other named forward workloads and the headline's backward pass."""
+    import synthetic
+    keys = {n if p == "fwd" else n + "_bwd" for n, p in bench.EXTRA_CONFIGS}
+    want = {w.name for w in synthetic.WORKLOADS + synthetic.FP8_WORKLOADS} - {
+        synthetic.HEADLINE.name}
+    assert want <= keys and synthetic.HEADLINE.name + "_bwd" in keys

@@ -24,10 +24,11 @@ def test_host_entry_matches_device_entry(shape, causal, dtype, chunks):
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     ho = torch.full(q.shape, float("nan"), dtype=q.dtype).pin_memory()
     hl = torch.full(q.shape[:3], float("nan"), dtype=torch.float32).pin_memory()
-    dq, dk, dv = (torch.empty(q.shape, dtype=q.dtype, device="cuda") for _ in range(3))
-    do_ = torch.empty(q.shape, dtype=q.dtype, device="cuda")
-    dl = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
-    wsa.fmha_fwd_host(hq, hk, hv, ho, hl, dq, dk, dv, do_, dl, causal=causal, scale=w.scale,
+    q_dev, k_dev, v_dev, o_dev = (torch.empty(q.shape, dtype=q.dtype, device="cuda")
+                                  for _ in range(4))
+    lse_dev = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    wsa.fmha_fwd_host(hq, hk, hv, ho, hl, q_dev, k_dev, v_dev, o_dev, lse_dev, causal=causal,
+                      scale=w.scale,
                       n_chunks=chunks)
     assert wsa.get_device_status() == wsa.FMHA_OK
     o_ref, l_ref = wsa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale)
@@ -41,10 +42,10 @@ def test_host_entry_pageable_memory_and_reuse():
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32)
     staging = [torch.empty(q.shape, dtype=q.dtype, device="cuda") for _ in range(4)]
-    dl = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    lse_dev = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
     o_ref, l_ref = wsa.attention(q.cuda(), k.cuda(), v.cuda(), scale=w.scale)
     for _ in range(2):  # the staging buffers and copy streams are reused
-        wsa.fmha_fwd_host(q, k, v, o, lse, *staging, dl, scale=w.scale, n_chunks=3)
+        wsa.fmha_fwd_host(q, k, v, o, lse, *staging, lse_dev, scale=w.scale, n_chunks=3)
         torch.cuda.synchronize()
         assert torch.equal(o, o_ref.cpu()) and torch.equal(lse, l_ref.cpu())
 

@@ -2,10 +2,12 @@
 
 Bar (per element, max abs over every compared element, outputs NaN-poisoned
 before each call): |O_gpu - O_oracle| <= 1e-2 and |LSE_gpu - LSE_oracle| <= 1e-3
-for N(0,1) inputs.  Small and ragged shapes are compared in full; the five
-named workloads are run at full size in the benchmark's launch configuration
-and compared on sampled rows of sampled heads (the oracle evaluates rows one
-by one), plus size-independent properties over every output.
+for N(0,1) inputs.  Small and ragged shapes are compared in full.  The named
+workloads run at full size in the benchmark's launch configuration: the four
+smaller ones are compared on every element; the headline one (B4 H32 S16384)
+on rows i = 0 (mod 8) plus the last 128 rows of every (batch, head) slice,
+which touches every work unit; all of them also pass size-independent
+properties over every output.
 """
 import math
 
@@ -108,19 +110,11 @@ def test_rising_maximum_forces_rescale(dt, causal, tau):
     assert eo <= tol_o and el <= TOL_LSE, "max err O %g LSE %g" % (eo, el)
 
 
-def _sample_rows(S, rng, n_random=48):
-    fixed = {0, 1, 2, 3, S - 1, S - 2, 127, 128, 129, 255, 256, 257}
-    rows = {r for r in fixed if 0 <= r < S}
-    rows |= set(rng.integers(0, S, size=n_random).tolist())
-    return np.array(sorted(rows), dtype=np.int64)
-
-
-@pytest.mark.parametrize("w", synthetic.WORKLOADS, ids=lambda w: w.name)
-def test_named_workload_sampled(w):
-    q, k, v = synthetic.make_inputs(w)
-    o, lse = _gpu(q, k, v, w.causal, w.scale)
-
-    # size-independent properties over every output
+def _size_independent_properties(w, q, k, v, o, lse):
+    """Checks that hold at any size, over every output element: finite
+    values, O inside the per-column range of V (a convex combination of V
+    rows, plus rounding slack), and under a causal mask LSE at least the
+    logit of the diagonal key (which every row sees)."""
     assert torch.isfinite(o).all().item() and torch.isfinite(lse).all().item()
     vd = v.cuda().float()
     vmax = vd.amax(dim=2, keepdim=True)
@@ -130,25 +124,57 @@ def test_named_workload_sampled(w):
     assert (of <= vmax + slack).all().item() and (of >= vmin - slack).all().item(), \
         "O is not inside the convex hull bound of V"
     if w.causal:
-        # LSE_i >= the logit of the diagonal key, which every causal row sees
         diag = (q.cuda().float() * k.cuda().float()).sum(-1) * w.scale
         assert (lse >= diag - 1e-3).all().item()
 
+
+@pytest.mark.parametrize("w", synthetic.WORKLOADS[:4], ids=lambda w: w.name)
+def test_named_workload_every_element(w):
+    """The four smaller named workloads at full size, in the benchmark's launch
+    configuration, compared with the oracle on every element of O and LSE
+    (the oracle evaluates all B*H*S rows: a few seconds of fp64 work for the
+    largest, B4 H32 S4096 causal)."""
+    q, k, v = synthetic.make_inputs(w)
+    o, lse = _gpu(q, k, v, w.causal, w.scale)
+    _size_independent_properties(w, q, k, v, o, lse)
+    o_ref, lse_ref = oracle.attention(q.double().numpy(), k.double().numpy(),
+                                      v.double().numpy(), w.causal, w.scale)
+    eo, el = _errors(o.cpu(), lse.cpu(), o_ref, lse_ref)
+    print("PARITY %s (every element) max_err_O %.3e max_err_LSE %.3e"
+          % (w.describe(), eo, el))
+    assert eo <= TOL_O and el <= TOL_LSE, "%s: max err O %g LSE %g" % (w.name, eo, el)
+
+
+def stratified_rows(S):
+    """Rows i = 0 (mod 8) plus the last 128 rows of a slice.  Every 256-row
+    work unit contributes 32 rows, spread over both 128-row query tiles and
+    all four 32-row lane quadrants of each, so a unit that was scheduled,
+    decoded or stored wrongly cannot pass."""
+    return np.union1d(np.arange(0, S, 8), np.arange(max(0, S - 128), S)).astype(np.int64)
+
+
+def test_headline_workload_stratified_rows_of_every_slice():
+    """The headline workload (B4 H32 S16384 D128 f16) in the benchmark's launch
+    configuration: the stratified rows of every one of the 128 (batch, head)
+    slices against the oracle -- 8192 work units, all of them checked,
+    including those adopted late by running blocks -- plus the size-independent
+    properties over every output."""
+    w = synthetic.HEADLINE
+    q, k, v = synthetic.make_inputs(w)
+    o, lse = _gpu(q, k, v, w.causal, w.scale)
+    _size_independent_properties(w, q, k, v, o, lse)
     o, lse = o.cpu(), lse.cpu()
-    rng = np.random.default_rng(w.seed)
-    BH = w.B * w.H
-    heads = sorted({0, BH // 2, BH - 1})
+    rows = stratified_rows(w.S)
     worst_o = worst_l = 0.0
-    for bh in heads:
+    for bh in range(w.B * w.H):
         b, h = divmod(bh, w.H)
-        rows = _sample_rows(w.S, rng)
         o_ref, lse_ref = oracle.attention_rows(
             q[b, h, rows].double().numpy(), k[b, h].double().numpy(),
             v[b, h].double().numpy(), rows, w.causal, w.scale)
         eo, el = _errors(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref)
         worst_o, worst_l = max(worst_o, eo), max(worst_l, el)
-    print("PARITY %s (sampled rows) max_err_O %.3e max_err_LSE %.3e"
-          % (w.describe(), worst_o, worst_l))
+    print("PARITY %s (%d rows x %d slices) max_err_O %.3e max_err_LSE %.3e"
+          % (w.describe(), rows.size, w.B * w.H, worst_o, worst_l))
     assert worst_o <= TOL_O and worst_l <= TOL_LSE, \
         "%s: max err O %g LSE %g" % (w.name, worst_o, worst_l)
 

@@ -203,3 +203,17 @@ def test_autograd_wrapper_matches_the_entry_points(causal, dtype):
     ulp = 2.0 ** -10 if dtype == torch.float16 else 2.0 ** -7
     diff = (qa.grad.float() - dq_r.float()).abs()
     assert bool((diff <= ulp * dq_r.float().abs() + 1e-5 * float(dq_r.float().abs().max())).all())
+
+
+def test_autograd_lse_output_is_not_differentiable():
+    """AttentionFunction returns LSE marked non-differentiable: O carries the
+    graph, LSE does not, and a backward through O alone needs no check of an
+    LSE gradient."""
+    w = synthetic.Workload("autograd-lse", 1, 2, 256, 64, "f16", True, 1.0, 4243)
+    q, k, v = (t.cuda().requires_grad_(True) for t in synthetic.make_inputs(w))
+    o, lse = wsa.AttentionFunction.apply(q, k, v, True, w.scale)
+    assert o.requires_grad and not lse.requires_grad
+    o.float().sum().backward()
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    for t in (q, k, v):
+        assert t.grad is not None and torch.isfinite(t.grad).all().item()

@@ -181,16 +181,18 @@ def fmha_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
         raise FmhaError(st, "fmha_fwd", lib.fmha_last_cuda_error().decode())
 
 
-def fmha_fwd_host(q, k, v, o, lse, dq, dk, dv, d_o, dlse, causal: bool = False,
+def fmha_fwd_host(q, k, v, o, lse, q_dev, k_dev, v_dev, o_dev, lse_dev, causal: bool = False,
                   scale: float | None = None, n_chunks: int = 0, stream=None) -> None:
     """Enqueue attention on host tensors with overlapped transfers (C ABI
     fmha_fwd_host): q, k, v, o (B, H, S, D) and lse (B, H, S) float32 are CPU
-    tensors (pinned for overlap); dq, dk, dv, d_o, dlse are CUDA staging
-    tensors of the same shapes.  Synchronise ``stream`` before reading o, lse.
+    tensors (pinned for overlap); q_dev, k_dev, v_dev, o_dev, lse_dev are CUDA
+    staging tensors of the same shapes and dtypes.  Synchronise ``stream``
+    before reading o, lse.
     """
     lib = load_library()
-    _check(dq, dk, dv, d_o, dlse)
-    for name, t, d in (("q", q, dq), ("k", k, dk), ("v", v, dv), ("o", o, d_o), ("lse", lse, dlse)):
+    _check(q_dev, k_dev, v_dev, o_dev, lse_dev)
+    for name, t, d in (("q", q, q_dev), ("k", k, k_dev), ("v", v, v_dev), ("o", o, o_dev),
+                       ("lse", lse, lse_dev)):
         if not isinstance(t, torch.Tensor) or t.is_cuda:
             raise ValueError("%s must be a CPU tensor" % name)
         if not t.is_contiguous() or t.shape != d.shape or t.dtype != d.dtype:
@@ -198,11 +200,11 @@ def fmha_fwd_host(q, k, v, o, lse, dq, dk, dv, d_o, dlse, causal: bool = False,
     B, H, S, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(dq.device):
+    with torch.cuda.device(q_dev.device):
         st = lib.fmha_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                               d_o.data_ptr(), dlse.data_ptr(), B, H, S, D, int(bool(causal)),
-                               float(scale), _dtype_code(q), int(n_chunks),
+                               lse.data_ptr(), q_dev.data_ptr(), k_dev.data_ptr(),
+                               v_dev.data_ptr(), o_dev.data_ptr(), lse_dev.data_ptr(), B, H, S, D,
+                               int(bool(causal)), float(scale), _dtype_code(q), int(n_chunks),
                                _stream_handle(stream))
     if st != FMHA_OK:
         raise FmhaError(st, "fmha_fwd_host", lib.fmha_last_cuda_error().decode())
@@ -361,7 +363,9 @@ class AttentionFunction(torch.autograd.Function):
     """Differentiable attention on the library's kernels: the forward runs
     fmha_fwd and keeps O and LSE, the backward runs fmha_bwd with them.
     16-bit (float16 / bfloat16) tensors of shape (B, H, S, D), D 64 or 128;
-    E4M3 inputs are forward-only."""
+    E4M3 inputs are forward-only.  LSE is returned as a non-differentiable
+    output: a loss that depends on it fails in the forward's autograd graph
+    (no gradient flows through it), not at backward time."""
 
     @staticmethod
     def forward(ctx, q, k, v, causal=False, scale=None):
@@ -370,12 +374,14 @@ class AttentionFunction(torch.autograd.Function):
         o, lse = attention(q, k, v, causal=causal, scale=scale)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.causal, ctx.scale = bool(causal), float(scale)
+        ctx.mark_non_differentiable(lse)
+        ctx.set_materialize_grads(False)
         return o, lse
 
     @staticmethod
     def backward(ctx, d_o, d_lse):
-        if d_lse is not None and bool(torch.any(d_lse != 0)):
-            raise NotImplementedError("gradients through the log-sum-exp output are not supported")
+        if d_o is None:   # O does not reach the loss: no gradient for q, k, v
+            return None, None, None, None, None
         q, k, v, o, lse = ctx.saved_tensors
         dq, dk, dv = attention_backward(q, k, v, o, lse, d_o.contiguous(), causal=ctx.causal,
                                         scale=ctx.scale)

@@ -356,13 +356,13 @@ fmha_status host_pipe(HostPipe** out) {
 }
 
 fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, float* lse,
-                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
+                          void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev, int64_t B,
                           int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
                           int n_chunks, void* stream) {
   if (!q || !k || !v || !o || !lse) return FMHA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return FMHA_ERR_INVALID_ARG;
   if (n_chunks < 0 || n_chunks > kMaxChunks) return FMHA_ERR_INVALID_ARG;
-  const fmha_status vs = validate(dq, dk, dv, d_o, dlse, B, H, S, D, scale, dtype);
+  const fmha_status vs = validate(q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
   const int64_t BH = B * H;
   // one (batch, head) slice of an input, of O and of LSE (V's transposed E4M3
@@ -400,26 +400,26 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
     const size_t off = static_cast<size_t>(s0) * slice, bytes = static_cast<size_t>(n) * slice;
     const size_t ooff = static_cast<size_t>(s0) * oslice, obytes = static_cast<size_t>(n) * oslice;
     const size_t loff = static_cast<size_t>(s0) * lslice, lbytes = static_cast<size_t>(n) * lslice;
-    if ((e = cudaMemcpyAsync(at(dq, off), at(q, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+    if ((e = cudaMemcpyAsync(at(q_dev, off), at(q, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
             cudaSuccess ||
-        (e = cudaMemcpyAsync(at(dk, off), at(k, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+        (e = cudaMemcpyAsync(at(k_dev, off), at(k, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
             cudaSuccess ||
-        (e = cudaMemcpyAsync(at(dv, off), at(v, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
+        (e = cudaMemcpyAsync(at(v_dev, off), at(v, off), bytes, cudaMemcpyHostToDevice, hp->h2d)) !=
             cudaSuccess ||
         (e = cudaEventRecord(hp->copied[c], hp->h2d)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(cs, hp->copied[c], 0)) != cudaSuccess)
       return cuda_fail(e, "host-to-device copy");
     // one (batch, head) range is a B = 1, H = n problem at offset pointers
     const fmha_status ks =
-        fwd_impl(at(dq, off), at(dk, off), at(dv, off), at(d_o, ooff),
-                 static_cast<float*>(at(dlse, loff)), 1, n, S, D, causal, scale, dtype, cs, 0,
+        fwd_impl(at(q_dev, off), at(k_dev, off), at(v_dev, off), at(o_dev, ooff),
+                 static_cast<float*>(at(lse_dev, loff)), 1, n, S, D, causal, scale, dtype, cs, 0,
                  kDefaultWaitLimitNs);
     if (ks != FMHA_OK) return ks;
     if ((e = cudaEventRecord(hp->computed[c], cs)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(at(o, ooff), at(d_o, ooff), obytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
+        (e = cudaMemcpyAsync(at(o, ooff), at(o_dev, ooff), obytes, cudaMemcpyDeviceToHost, hp->d2h)) !=
             cudaSuccess ||
-        (e = cudaMemcpyAsync(at(lse, loff), at(dlse, loff), lbytes, cudaMemcpyDeviceToHost,
+        (e = cudaMemcpyAsync(at(lse, loff), at(lse_dev, loff), lbytes, cudaMemcpyDeviceToHost,
                              hp->d2h)) != cudaSuccess)
       return cuda_fail(e, "device-to-host copy");
   }
@@ -573,10 +573,10 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
 }
 
 fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
-                          void* dq, void* dk, void* dv, void* d_o, float* dlse, int64_t B,
-                          int64_t H, int64_t S, int64_t D, int causal, float scale,
+                          void* q_dev, void* k_dev, void* v_dev, void* o_dev, float* lse_dev,
+                          int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
                           fmha_dtype dtype, int n_chunks, void* stream) {
-  return fwd_host_impl(q, k, v, o, lse, dq, dk, dv, d_o, dlse, B, H, S, D, causal, scale,
+  return fwd_host_impl(q, k, v, o, lse, q_dev, k_dev, v_dev, o_dev, lse_dev, B, H, S, D, causal, scale,
                        static_cast<int>(dtype), n_chunks, stream);
 }
 
