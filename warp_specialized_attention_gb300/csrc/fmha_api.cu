@@ -38,6 +38,24 @@ fmha_status cuda_fail(cudaError_t e, const char* what) {
   return FMHA_ERR_CUDA;
 }
 
+// A driver-API failure (the tensor-map encoder), with the driver's own code.
+fmha_status drv_fail(CUresult r, const char* what) {
+  std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: CUresult %d", what,
+                static_cast<int>(r));
+  return FMHA_ERR_CUDA;
+}
+
+// Makes the current device's primary context current on the calling host
+// thread.  The driver-API tensor-map encoder needs a current context, and a
+// thread that has not yet made a runtime call (a framework's worker thread,
+// for instance) has none; cudaSetDevice initialises and binds it.
+fmha_status bind_context() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
+  return e == cudaSuccess ? FMHA_OK : cuda_fail(e, "cudaSetDevice");
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -66,8 +84,8 @@ EncodeTiledFn encode_fn(cudaError_t* err) {
 // (64 16-bit or 128 8-bit elements) x 128 rows x 1 head, 128-byte swizzle.
 // Rows past the end read as zeros.  Q, K, V: rows = S, cols = D; the
 // transposed E4M3 V: rows = D, cols = S.
-bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype, int64_t BH,
-                int64_t rows, int64_t cols) {
+CUresult encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype, int64_t BH,
+                    int64_t rows, int64_t cols) {
   const int64_t eb = dtype == FMHA_E4M3 ? 1 : 2;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(BH)};
@@ -81,13 +99,31 @@ bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dtype,
   const CUresult r = enc(map, t, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return r;
+}
+
+// O (B*H, S, D) in its 16-bit output type for the forward epilogue's TMA
+// stores: boxes of 64 columns (128 bytes) x 32 rows (one softmax warp's rows)
+// x 1 head, 128-byte swizzle; rows past S are not written.
+CUresult encode_o_map(EncodeTiledFn enc, CUtensorMap* map, void* ptr, bool bf16, int64_t BH,
+                      int64_t S, int64_t D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 2),
+                                 static_cast<cuuint64_t>(S * D * 2)};
+  const cuuint32_t box[3] = {64, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r;
 }
 
 // The backward's fp32 dQ accumulator (B*H, S, D): boxes of 32 rows x 16
 // columns (64 bytes), 64-byte swizzle, for the kernel's TMA reduce-adds.
-bool encode_dq_map(EncodeTiledFn enc, CUtensorMap* map, float* ptr, int64_t BH, int64_t S,
-                   int64_t D) {
+CUresult encode_dq_map(EncodeTiledFn enc, CUtensorMap* map, float* ptr, int64_t BH, int64_t S,
+                       int64_t D) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D * 4),
@@ -97,7 +133,7 @@ bool encode_dq_map(EncodeTiledFn enc, CUtensorMap* map, float* ptr, int64_t BH, 
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return r;
 }
 
 // Bytes per element of the inputs and of O.
@@ -173,22 +209,27 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   const fmha_status vs = validate(q, k, v, o, lse, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
 
+  const fmha_status bs = bind_context();
+  if (bs != FMHA_OK) return bs;
   cudaError_t e;
   EncodeTiledFn enc = encode_fn(&e);
   if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
   const bool bf16 = dtype == FMHA_BF16, e4m3 = dtype == FMHA_E4M3;
   const int64_t BH = B * H;
-  alignas(64) CUtensorMap tq, tk, tv;
-  if (!encode_map(enc, &tq, q, dtype, BH, S, D) || !encode_map(enc, &tk, k, dtype, BH, S, D) ||
-      !(e4m3 ? encode_map(enc, &tv, v, dtype, BH, D, S) : encode_map(enc, &tv, v, dtype, BH, S, D)))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  alignas(64) CUtensorMap tq, tk, tv, to;
+  CUresult r;
+  if ((r = encode_map(enc, &tq, q, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = encode_map(enc, &tk, k, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = e4m3 ? encode_map(enc, &tv, v, dtype, BH, D, S)
+                : encode_map(enc, &tv, v, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = encode_o_map(enc, &to, o, bf16 || e4m3, BH, S, D)) != CUDA_SUCCESS)
+    return drv_fail(r, "cuTensorMapEncodeTiled");
 
   int* status = nullptr;
   e = status_word(&status);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
 
   wsa::FwdParams prm;
-  prm.o = o;
   prm.lse = lse;
   prm.status = status;
   prm.S = static_cast<int>(S);
@@ -210,9 +251,9 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   const unsigned grid = static_cast<unsigned>(prm.n_qblk * BH);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  e = e4m3      ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, prm, grid, st)
-      : D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, prm, grid, st)
-                : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, prm, grid, st);
+  e = e4m3      ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, to, prm, grid, st)
+      : D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, to, prm, grid, st)
+                : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, to, prm, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return FMHA_OK;
 }
@@ -265,21 +306,26 @@ fmha_status bwd_enqueue(const void* q, const void* k, const void* v, const void*
                         float* dq_acc, float* delta, int64_t BH, int64_t S, int64_t D, int causal,
                         float scale, int dtype, cudaStream_t st, uint64_t wait_limit_ns) {
   const int64_t n_blk = (S + 127) / 128;
+  const fmha_status bs = bind_context();
+  if (bs != FMHA_OK) return bs;
   cudaError_t e;
   EncodeTiledFn enc = encode_fn(&e);
   if (!enc) return cuda_fail(e, "cuTensorMapEncodeTiled entry point");
   alignas(64) CUtensorMap tq, tk, tv, tdo;
-  if (!encode_map(enc, &tq, q, dtype, BH, S, D) || !encode_map(enc, &tk, k, dtype, BH, S, D) ||
-      !encode_map(enc, &tv, v, dtype, BH, S, D) || !encode_map(enc, &tdo, d_o, dtype, BH, S, D))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  CUresult r;
+  if ((r = encode_map(enc, &tq, q, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = encode_map(enc, &tk, k, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = encode_map(enc, &tv, v, dtype, BH, S, D)) != CUDA_SUCCESS ||
+      (r = encode_map(enc, &tdo, d_o, dtype, BH, S, D)) != CUDA_SUCCESS)
+    return drv_fail(r, "cuTensorMapEncodeTiled");
   int* status = nullptr;
   if ((e = status_word(&status)) != cudaSuccess)
     return cuda_fail(e, "cudaGetSymbolAddress(status)");
 
   const bool bf16 = dtype == FMHA_BF16;
   alignas(64) CUtensorMap tdq;
-  if (!encode_dq_map(enc, &tdq, dq_acc, BH, S, D))
-    return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(dQ accumulator)");
+  if ((r = encode_dq_map(enc, &tdq, dq_acc, BH, S, D)) != CUDA_SUCCESS)
+    return drv_fail(r, "cuTensorMapEncodeTiled(dQ accumulator)");
   if ((e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(BH * S * D) * 4, st)) != cudaSuccess)
     return cuda_fail(e, "clear the dQ accumulator");
   if ((e = wsa::launch_bwd_delta(static_cast<int>(D), bf16, o, d_o, delta, BH * S, st)) !=

@@ -5,13 +5,13 @@
 namespace wsa {
 
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& prm,
+                           unsigned grid, cudaStream_t stream) {
   if (bf16)
-    return causal ? launch_fmha_fwd<64, kBF16, true>(tq, tk, tv, prm, grid, stream)
-                  : launch_fmha_fwd<64, kBF16, false>(tq, tk, tv, prm, grid, stream);
-  return causal ? launch_fmha_fwd<64, kF16, true>(tq, tk, tv, prm, grid, stream)
-                : launch_fmha_fwd<64, kF16, false>(tq, tk, tv, prm, grid, stream);
+    return causal ? launch_fmha_fwd<64, kBF16, true>(tq, tk, tv, to, prm, grid, stream)
+                  : launch_fmha_fwd<64, kBF16, false>(tq, tk, tv, to, prm, grid, stream);
+  return causal ? launch_fmha_fwd<64, kF16, true>(tq, tk, tv, to, prm, grid, stream)
+                : launch_fmha_fwd<64, kF16, false>(tq, tk, tv, to, prm, grid, stream);
 }
 
 }  // namespace wsa

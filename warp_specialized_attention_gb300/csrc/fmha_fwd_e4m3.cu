@@ -6,10 +6,10 @@
 namespace wsa {
 
 cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tvt, const FwdParams& prm, unsigned grid,
+                            const CUtensorMap& tvt, const CUtensorMap& to, const FwdParams& prm, unsigned grid,
                             cudaStream_t stream) {
-  return causal ? launch_fmha_fwd<128, kE4M3, true>(tq, tk, tvt, prm, grid, stream)
-                : launch_fmha_fwd<128, kE4M3, false>(tq, tk, tvt, prm, grid, stream);
+  return causal ? launch_fmha_fwd<128, kE4M3, true>(tq, tk, tvt, to, prm, grid, stream)
+                : launch_fmha_fwd<128, kE4M3, false>(tq, tk, tvt, to, prm, grid, stream);
 }
 
 }  // namespace wsa

@@ -111,8 +111,18 @@ struct Cfg {
   static constexpr int kColBlocks = D * kElemBytes / 128;  // 128-byte column blocks of a row
   static constexpr int kQBytes = 2 * kTileBytes;
   static constexpr int kRingOff = kQBytes;
-  static constexpr int kCtlOff = kRingOff + kStages * kSlotBytes;
+  // O staging for the epilogue's TMA stores: per softmax warp, kStageBoxes
+  // boxes of 32 rows x 128 bytes (64 16-bit columns of O), 128-byte swizzle.
+  // O rows have kOutColBlocks such boxes; with fewer staging boxes than that
+  // (16-bit D = 128, where shared memory holds one box per warp) a box is
+  // refilled once the TMA engine has read the previous one.
+  static constexpr int kOutColBlocks = D * 2 / 128;
+  static constexpr int kStageBoxes = ET == kE4M3 ? 2 : 1;
+  static constexpr int kStageBoxBytes = 32 * 128;
+  static constexpr int kStageOff = kRingOff + kStages * kSlotBytes;
+  static constexpr int kCtlOff = kStageOff + 8 * kStageBoxes * kStageBoxBytes;
   static constexpr int kSmemBytes = 1024 + kCtlOff + 512;  // + alignment slack + control
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
   static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
   // D = 64 leaves 128 TMEM columns free: P_t gets its own 64 columns there
   // (split P), so S_t can be overwritten as soon as the softmax has read it.
@@ -145,8 +155,7 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= 512, "control block size");
 
 struct FwdParams {
-  void* o;            // (B,H,S,D) 16-bit
-  float* lse;         // (B,H,S) fp32
+  float* lse;         // (B,H,S) fp32 (O is written through its tensor map)
   int* status;        // device status word
   int S;
   int n_qblk;         // ceil(S / 256)
@@ -406,7 +415,8 @@ template <int D, int ET, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using C = Cfg<D, ET>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles
@@ -461,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t sQ = sbase;
   const uint32_t sRing = sbase + C::kRingOff;
+  const uint32_t sStage = sbase + C::kStageOff;
 
   // The k-th unit of this block (k = 0, 1, ...) travels from the loader to the
   // other roles through slot k & 1 of the unit channel; -1 ends the loop.
@@ -909,7 +920,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       g += nkv;
 
       // ---- epilogue: O / l in the output dtype (the input's, bf16 for E4M3
-      // inputs), LSE = ln 2 * (m + log2 l - p_shift)
+      // inputs), LSE = ln 2 * (m + log2 l - p_shift).  Per 64-column block of
+      // O_t each warp reads its 32 rows out of TMEM in two 32-column loads,
+      // scales and packs them into its shared-memory staging box (128-byte
+      // swizzle, so the 8 lanes of a quarter-warp store to 8 different 16-byte
+      // bank groups), and one lane stores the box with a TMA tensor store:
+      // whole 128-byte row segments, no per-row global stores; the store runs
+      // while the warp moves on (Tawa, Section IV-B, Fig. 7(b): the epilogue
+      // of one tile overlaps the next tile's loads and MMAs).  O_t is released
+      // once its last columns are in registers.  Reading all of O_t in one
+      // burst instead was 9 % slower on causal workloads, where this tile's
+      // epilogue runs beside the other tile's last softmax block.
       if (ok) {
         ok = mbar_wait(&ctl.o_full[t], k & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
                        p.wait_limit_ns);
@@ -918,33 +939,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const bool store = row < S;
-      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      ((static_cast<size_t>(u.bh) * S + (store ? row : 0)) * D) * 2;
+      const int row0 = u.qb * 2 * kBM + t * kBM + quad * 32;  // the warp's first row
+      const uint32_t stage = sStage + warp * (C::kStageBoxes * C::kStageBoxBytes);
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t orr[32];
-        tmem_ld_x32(tO + ch * 32, orr);
-        uint32_t pkd[16];
+      for (int cb = 0; cb < C::kOutColBlocks; ++cb) {
+        const uint32_t box = stage + (cb % C::kStageBoxes) * C::kStageBoxBytes;
+        // the box's previous TMA store has finished reading it
+        if (lane == 0) bulk_wait_group_read<C::kStageBoxes - 1>();
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pkd[i] = pack2<ET != kF16>(__uint_as_float(orr[2 * i]) * inv_l,
-                               __uint_as_float(orr[2 * i + 1]) * inv_l);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + ch * 64);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t orr[32];
+          tmem_ld_x32(tO + cb * 64 + h * 32, orr);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = h * 4 + c4;
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w4[i] = pack2<ET != kF16>(__uint_as_float(orr[c4 * 8 + 2 * i]) * inv_l,
+                                        __uint_as_float(orr[c4 * 8 + 2 * i + 1]) * inv_l);
+            st_shared_v4(box + lane * 128 + ((c ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async_smem();  // this lane's writes, visible to the TMA engine
+        __syncwarp();
+        if (lane == 0) {
+          if (row0 < S) tma_store_3d(&tm_o, box, cb * 64, row0, u.bh);  // rows >= S clipped
+          bulk_commit_group();
         }
       }
       // O_t has left TMEM: the next unit's first P V may overwrite it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.o_empty[t]);
-      if (store)
+      if (row < S)
         p.lse[static_cast<size_t>(u.bh) * S + row] =
             (m + lg2(l) - shift) * 0.69314718055994530942f;
     }
+    // every TMA store of O has completed before the block may exit
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   // ---- teardown: every role has drained its asynchronous work
@@ -962,7 +997,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // process-wide symbol shared by every copy).
 template <int D, int ET, bool CAUSAL>
 static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdParams& prm, unsigned grid, cudaStream_t stream) {
+                            const CUtensorMap& to, const FwdParams& prm, unsigned grid,
+                            cudaStream_t stream) {
   auto kern = fmha_fwd_kernel<D, ET, CAUSAL>;
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> opted_in[kMaxDevices];
@@ -975,7 +1011,7 @@ static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, prm);
+  kern<<<grid, kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
   return cudaGetLastError();
 }
 

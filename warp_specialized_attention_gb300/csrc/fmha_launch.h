@@ -12,17 +12,19 @@ struct FwdParams;
 struct BwdParams;
 
 // Enqueue the forward kernel for one (head dim, dtype, mask) variant.
+// `to` maps O (D, S, B*H) in 16-bit boxes of 64 columns x 32 rows, 128-byte
+// swizzle, for the epilogue's TMA stores.
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
-                           cudaStream_t stream);
+                           const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& prm,
+                           unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const FwdParams& prm, unsigned grid,
-                            cudaStream_t stream);
+                            const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& prm,
+                            unsigned grid, cudaStream_t stream);
 
-// E4M3 inputs, head dim 128: tvt maps V transposed, (S, D, B*H).
+// E4M3 inputs, head dim 128: tvt maps V transposed, (S, D, B*H); O is bf16.
 cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tvt, const FwdParams& prm, unsigned grid,
-                            cudaStream_t stream);
+                            const CUtensorMap& tvt, const CUtensorMap& to, const FwdParams& prm,
+                            unsigned grid, cudaStream_t stream);
 
 // Backward pass (16-bit, D = 64 or 128): the main kernel over (head, key
 // block), the delta pre-pass over rows, and the dQ conversion of n elements.

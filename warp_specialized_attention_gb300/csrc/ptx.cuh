@@ -337,6 +337,35 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
       : "memory");
 }
 
+// 3-D tiled bulk tensor store shared (this CTA) -> global: the box at
+// (c0, c1, c2) is written from src_smem; rows of the box outside the tensor are
+// skipped.  Completion is tracked by the issuing thread's bulk async-group.
+// c0 x element size must be a multiple of 16 bytes and no coordinate may be
+// negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src_smem, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src_smem), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Waits until at most N of this thread's committed bulk groups are still
+// reading their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// One 16-byte shared-memory store.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
