@@ -16,13 +16,18 @@ The model mirrors, role by role, the barrier program of
 warp_specialized_attention_gb300/csrc/fmha_fwd_sm103.cuh:
 
   producer   unit channel (unit_full/unit_empty), K_j/V_j through a ring
-             (kv_full/kv_empty), Q after K_0/V_0 of each unit (q_full/q_empty)
-  MMA        Q K^T and P V issue with tcgen05.commit arrivals; the head-dim 128
-             schedule (P over S) and the head-dim 64 one (split P: s_free,
-             pva_done/pvb_done)
+             (kv_full, and one kv_empty per query tile: a slot is reloaded
+             once every tile that read its previous item has released it),
+             Q_t after K_0/V_0 of each unit (q_full[t]/q_empty[t])
+  MMA        the head-dim 128 schedule (P over S): one issuer for both tiles
+             in the order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1), releasing
+             every ring item and both Q tiles; the head-dim 64 one (split P:
+             s_free, pva_done/pvb_done): one issuer per query tile, each
+             releasing the ring items and the Q tile its tile read
   softmax    4 warps per query tile: S wait, P releases in two halves, the
              rescale waits, epilogue (o_full/o_empty)
-  tensor     commits complete in issue order after random delays
+  tensor     each issuer's commits complete in its own issue order after
+             random delays; two issuers' commits interleave freely
   TMA        copies complete in any order after random delays
 
 Barrier semantics are the hardware's: a wait for parity p passes iff the
@@ -57,22 +62,23 @@ class Model:
         self.stages = stages
         self.errors = []
         self.bars = {}
-        self.tensor_q = []           # pending commits, completed in order
         self.tma_q = []              # pending copies, completed in any order
+        self.tensor_q = [[], []]     # per issuer: pending commits, completed in order
         b = self.bar
         for i in range(2):
             b(("unit_full", i), 1)
-            b(("unit_empty", i), 9)
-        b("q_full", 1)
-        b("q_empty", 1)
+            b(("unit_empty", i), 10 if split else 9)   # issuers + eight softmax warps
         for t in range(2):
             for n, c in (("s_full", 1), ("p0", 4), ("p1", 4), ("pva", 1), ("pvb", 1),
-                         ("s_free", 4), ("o_full", 1), ("o_empty", 4)):
+                         ("s_free", 4), ("o_full", 1), ("o_empty", 4), ("q_full", 1),
+                         ("q_empty", 1)):
                 b((n, t), c)
         for s in range(stages):
             b(("kv_full", s), 1)
-            b(("kv_empty", s), 1)
+            for t in range(2):
+                b(("kv_empty", t, s), 1)
         self.unit_slot = [None, None]
+        self.slot_item = [None] * stages   # which ring item each slot holds (set when a copy lands)
 
     def bar(self, name, count):
         self.bars[name] = Bar(count)
@@ -86,15 +92,25 @@ class Model:
             self.errors.append("wait on %s passed for phase %d with %d phases done"
                                % (name, index, bar.done))
 
-    def commit(self, name):
-        self.tensor_q.append(name)
+    def commit(self, t, name):
+        self.tensor_q[t].append(name)
 
-    def copy(self, name):
-        self.tma_q.append(name)
+    def copy(self, name, item=None):
+        self.tma_q.append((name, item))
+
+    def check_slot(self, t, item, what):
+        """The ring slot of `item` must still hold it when tile t's MMAs read or release it."""
+        slot = item % self.stages
+        if self.slot_item[slot] != item:
+            self.errors.append("tile %d %s item %d but slot %d holds item %s"
+                               % (t, what, item, slot, self.slot_item[slot]))
 
     # ------------------------------------------------------------------ roles
     def producer(self):
-        it = nq = 0
+        it = 0
+        nq = [0, 0]
+        mask = [0] * self.stages          # tiles that read the item now in each slot
+        uses = [[0] * self.stages for _ in range(2)]   # items of each slot each tile read
         for k in range(len(self.units) + 1):
             if k >= 2:   # the consumers have read the unit that used this slot before
                 yield from self.wait(("unit_empty", k & 1), (k >> 1) - 1)
@@ -102,19 +118,26 @@ class Model:
             self.bars[("unit_full", k & 1)].arrive()
             if k == len(self.units):
                 return
-            n1 = self.units[k][1]
+            n0, n1 = self.units[k]
             for j in range(n1):
                 for kv in range(2):
-                    slot, use = it % self.stages, it // self.stages
-                    if use > 0:
-                        yield from self.wait(("kv_empty", slot), use - 1)
-                    self.copy(("kv_full", slot))
+                    slot = it % self.stages
+                    for t in range(2):
+                        if mask[slot] >> t & 1:
+                            yield from self.wait(("kv_empty", t, slot), uses[t][slot] - 1)
+                    # one issuer releases every item (as issuer 0); two
+                    # issuers release the items their own tile read
+                    mask[slot] = (2 | (1 if j < n0 else 0)) if self.split else 1
+                    for t in range(2):
+                        uses[t][slot] += mask[slot] >> t & 1
+                    self.copy(("kv_full", slot), it)
                     it += 1
                     if j == 0 and kv == 1:
-                        if nq > 0:
-                            yield from self.wait("q_empty", nq - 1)
-                        self.copy("q_full")
-                        nq += 1
+                        for t in range(2):
+                            if nq[t] > 0:
+                                yield from self.wait(("q_empty", t), nq[t] - 1)
+                            self.copy(("q_full", t))
+                            nq[t] += 1
 
     def next_unit(self, k):
         yield from self.wait(("unit_full", k & 1), k >> 1)
@@ -122,7 +145,63 @@ class Model:
         self.bars[("unit_empty", k & 1)].arrive()
         return u
 
-    def mma(self):
+    def mma_tile(self, t):
+        """The issuer of query tile t (split P)."""
+        it = g = 0
+        k = 0
+        while True:
+            u = yield from self.next_unit(k)
+            if u < 0:
+                return
+            n = self.units[u][t]
+            n1 = self.units[u][1]
+            K = lambda j: it + 2 * j
+            V = lambda j: it + 2 * j + 1
+            full = lambda item: self.wait(("kv_full", item % self.stages), item // self.stages)
+            release = lambda item: self.commit(t, ("release", t, item))
+
+            def use(item):
+                yield from full(item)
+                self.check_slot(t, item, "reads")
+            yield from use(K(0))
+            yield from self.wait(("q_full", t), k)
+            if self.split and g > 0:
+                yield from self.wait(("s_free", t), g - 1)
+            self.commit(t, ("s_full", t))
+            release(K(0))
+            if n == 1:
+                self.commit(t, ("q_empty", t))
+            if k > 0:
+                yield from self.wait(("o_empty", t), k - 1)
+            for j in range(n):
+                if self.split and j + 1 < n:
+                    yield from use(K(j + 1))
+                    yield from self.wait(("s_free", t), g + j)
+                    self.commit(t, ("s_full", t))
+                    release(K(j + 1))
+                    if j + 2 == n:
+                        self.commit(t, ("q_empty", t))
+                yield from use(V(j))
+                yield from self.wait(("p0", t), g + j)
+                self.commit(t, ("pva", t))
+                yield from self.wait(("p1", t), g + j)
+                if self.split:
+                    self.commit(t, ("pvb", t))
+                release(V(j))
+                if j == n - 1:
+                    self.commit(t, ("o_full", t))
+                if not self.split and j + 1 < n:
+                    yield from use(K(j + 1))
+                    self.commit(t, ("s_full", t))
+                    release(K(j + 1))
+                    if j + 2 == n:
+                        self.commit(t, ("q_empty", t))
+            it += 2 * n1
+            g += n
+            k += 1
+
+    def mma_single(self):
+        """One issuer for both tiles (P over S)."""
         it = g0 = g1 = 0
         k = 0
         while True:
@@ -133,74 +212,52 @@ class Model:
             K = lambda j: it + 2 * j
             V = lambda j: it + 2 * j + 1
             full = lambda item: self.wait(("kv_full", item % self.stages), item // self.stages)
-            yield from full(K(0))
-            yield from self.wait("q_full", k)
+            release = lambda item: self.commit(0, ("release", 0, item))
+
+            def use(item):
+                yield from full(item)
+                self.check_slot(0, item, "reads")
 
             def pv(t, g, j):
                 yield from self.wait(("p0", t), g + j)
-                self.commit(("pva", t))
+                self.commit(0, ("pva", t))
                 yield from self.wait(("p1", t), g + j)
-                if self.split:
-                    self.commit(("pvb", t))
 
-            if self.split:
-                if g0 > 0:
-                    yield from self.wait(("s_free", 0), g0 - 1)
-                self.commit(("s_full", 0))
-                if g1 > 0:
-                    yield from self.wait(("s_free", 1), g1 - 1)
-                self.commit(("s_full", 1))
-            else:
-                self.commit(("s_full", 0))
-                self.commit(("s_full", 1))
-            self.commit(("kv_empty", K(0) % self.stages))
+            def free_q():
+                self.commit(0, ("q_empty", 0))
+                self.commit(0, ("q_empty", 1))
+
+            yield from use(K(0))
+            yield from self.wait(("q_full", 0), k)
+            yield from self.wait(("q_full", 1), k)
+            self.commit(0, ("s_full", 0))
+            self.commit(0, ("s_full", 1))
+            release(K(0))
             if n1 == 1:
-                self.commit("q_empty")
+                free_q()
             if k > 0:
                 yield from self.wait(("o_empty", 0), k - 1)
                 yield from self.wait(("o_empty", 1), k - 1)
             for j in range(n1):
                 more = j + 1 < n1
-                if self.split:
+                yield from use(V(j))
+                if j < n0:
+                    yield from pv(0, g0, j)
+                    if j == n0 - 1:
+                        self.commit(0, ("o_full", 0))
+                if more:
+                    yield from use(K(j + 1))
                     if j + 1 < n0:
-                        yield from full(K(j + 1))
-                        yield from self.wait(("s_free", 0), g0 + j)
-                        self.commit(("s_full", 0))
-                    yield from full(V(j))
-                    if j < n0:
-                        yield from pv(0, g0, j)
-                        if j == n0 - 1:
-                            self.commit(("o_full", 0))
-                    if more:
-                        yield from full(K(j + 1))
-                        yield from self.wait(("s_free", 1), g1 + j)
-                        self.commit(("s_full", 1))
-                        self.commit(("kv_empty", K(j + 1) % self.stages))
-                        if j + 2 == n1:
-                            self.commit("q_empty")
-                    yield from pv(1, g1, j)
-                    self.commit(("kv_empty", V(j) % self.stages))
-                    if j == n1 - 1:
-                        self.commit(("o_full", 1))
-                else:
-                    yield from full(V(j))
-                    if j < n0:
-                        yield from pv(0, g0, j)
-                        if j == n0 - 1:
-                            self.commit(("o_full", 0))
-                    if more:
-                        yield from full(K(j + 1))
-                        if j + 1 < n0:
-                            self.commit(("s_full", 0))
-                    yield from pv(1, g1, j)
-                    self.commit(("kv_empty", V(j) % self.stages))
-                    if j == n1 - 1:
-                        self.commit(("o_full", 1))
-                    if more:
-                        self.commit(("s_full", 1))
-                        self.commit(("kv_empty", K(j + 1) % self.stages))
-                        if j + 2 == n1:
-                            self.commit("q_empty")
+                        self.commit(0, ("s_full", 0))
+                yield from pv(1, g1, j)
+                release(V(j))
+                if j == n1 - 1:
+                    self.commit(0, ("o_full", 1))
+                if more:
+                    self.commit(0, ("s_full", 1))
+                    release(K(j + 1))
+                    if j + 2 == n1:
+                        free_q()
             it += 2 * n1
             g0 += n0
             g1 += n1
@@ -244,14 +301,25 @@ class Model:
         in any order."""
         while True:
             r = self.rng.random()
-            if self.tensor_q and r < 0.5:
-                self.bars[self.tensor_q.pop(0)].arrive()
+            queues = [q for q in self.tensor_q if q]
+            if queues and r < 0.5:
+                name = self.rng.choice(queues).pop(0)
+                if name[0] == "release":   # tile t's MMAs reading this item have completed
+                    _, t, item = name
+                    self.check_slot(t, item, "released")
+                    self.bars[("kv_empty", t, item % self.stages)].arrive()
+                else:
+                    self.bars[name].arrive()
             elif self.tma_q and r >= 0.5:
-                self.bars[self.tma_q.pop(self.rng.randrange(len(self.tma_q)))].arrive()
+                name, item = self.tma_q.pop(self.rng.randrange(len(self.tma_q)))
+                if name[0] == "kv_full":
+                    self.slot_item[name[1]] = item
+                self.bars[name].arrive()
             yield
 
     def run(self, max_idle=20000):
-        roles = [self.producer(), self.mma()] + [self.softmax(t) for t in range(2) for _ in range(4)]
+        issuers = [self.mma_tile(0), self.mma_tile(1)] if self.split else [self.mma_single()]
+        roles = [self.producer()] + issuers + [self.softmax(t) for t in range(2) for _ in range(4)]
         engines = self.engines()
         alive = list(roles)
         idle = 0
@@ -266,7 +334,7 @@ class Model:
                 idle = 0
             if self.errors:
                 return "false pass: " + self.errors[0]
-            if idle > max_idle and not self.tensor_q and not self.tma_q:
+            if idle > max_idle and not any(self.tensor_q) and not self.tma_q:
                 return "deadlock"
         n = len(self.units)
         for t in range(2):
@@ -319,3 +387,20 @@ def test_model_detects_a_false_parity_pass():
     with pytest.raises(StopIteration):
         next(m.wait(("o_full", 0), 2))
     assert m.errors and "phase 2" in m.errors[0]
+
+
+def test_model_detects_a_slot_reloaded_before_a_tile_released_it():
+    """Negative control: a producer that waits only for tile 1's release of a
+    ring slot reloads it while tile 0's MMAs may still read the old item."""
+    class OneTileEmpty(Model):
+        def wait(self, name, index):
+            if name[0] == "kv_empty" and name[1] == 0:
+                return iter(())            # the dropped wait
+            return Model.wait(self, name, index)
+    bad = 0
+    for seed in range(200):
+        rng = random.Random(seed)
+        units = _units(rng, True, rng.randint(2, 5))
+        if OneTileEmpty(units, True, 8, seed, True).run() != "ok":
+            bad += 1
+    assert bad > 0

@@ -80,9 +80,9 @@ namespace wsa {
 
 constexpr int kBM = 128;       // query rows per tile (tcgen05 M)
 constexpr int kBN = 128;       // keys per block
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kWarpMma = 8;
+constexpr int kWarpMma = 8;    // MMA issuer (of query tile 0 with two issuers) and TMEM allocator
 constexpr int kWarpLoad = 9;
+constexpr int kWarpMma1 = 10;  // MMA issuer of query tile 1 (with two issuers)
 constexpr float kTauDefault = 15.0f;     // lazy-rescale threshold, log2 units (16-bit P)
 constexpr float kTauDefaultE4m3 = 8.0f;  // E4M3 P: stored unscaled, <= 2^8 = 256 < 448
 constexpr uint32_t kTmemCols = 512;
@@ -129,6 +129,15 @@ struct Cfg {
   static constexpr bool kSplitP = D == 64 && ET != kE4M3;
   static constexpr uint32_t kPCol = 256 + 2 * D;           // split P_t at kPCol + 64t
   static_assert(!kSplitP || kPCol + 128 <= 512, "TMEM columns");
+  // MMA issuers.  At D = 128 one warp issues both tiles' MMAs in the order
+  // P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): that order keeps the two tiles
+  // half a block period apart, so one tile's softmax runs while the other
+  // tile's MMAs do.  With split P (D = 64) the tiles' softmax phases overlap
+  // anyway, and one issuer per tile keeps a wait on one tile from holding up
+  // the other tile's MMAs.
+  static constexpr int kIssuers = kSplitP ? 2 : 1;
+  static constexpr int kThreads = kIssuers == 2 ? 352 : 320;  // 11 or 10 warps
+  static constexpr int kUnitReaders = 8 + kIssuers;           // softmax warps + issuers
 };
 
 struct Ctl {
@@ -137,8 +146,8 @@ struct Ctl {
   uint64_t unit_full[2];   // work-unit channel, loader -> MMA and softmax warps
   uint64_t unit_empty[2];
   int unit_id[2];          // unit index, or -1: no more work
-  uint64_t q_full;
-  uint64_t q_empty;        // Q tiles consumed by the unit's last Q K^T
+  uint64_t q_full[2];      // [tile]
+  uint64_t q_empty[2];     // [tile]: Q_t consumed by the unit's last Q_t K^T
   uint64_t s_full[2];
   uint64_t p_half[2][2];   // [tile][key half]: P of keys 64h..64h+63 is in TMEM
   uint64_t pva_done[2];    // [tile]: the P V of keys 0-63 of the current block is done
@@ -146,9 +155,9 @@ struct Ctl {
   uint64_t s_free[2];      // [tile]: the softmax has read S_t (split P only)
   uint64_t o_full[2];
   uint64_t o_empty[2];     // [tile]: the epilogue has read O_t out of TMEM
-  uint64_t mma_drain;
+  uint64_t mma_drain[2];
   uint64_t kv_full[8];
-  uint64_t kv_empty[8];
+  uint64_t kv_empty[2][8]; // [tile][slot]: that tile's MMAs have finished reading the slot
   uint32_t tmem_base;
   int abort;
 };
@@ -412,7 +421,7 @@ __device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, flo
 }
 
 template <int D, int ET, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
@@ -437,11 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl.clc_bar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.unit_full[i], 1);
-      mbar_init(&ctl.unit_empty[i], 9);  // the MMA warp and the 8 softmax warps
+      mbar_init(&ctl.unit_empty[i], C::kUnitReaders);
     }
-    mbar_init(&ctl.q_full, 1);
-    mbar_init(&ctl.q_empty, 1);
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctl.q_full[t], 1);
+      mbar_init(&ctl.q_empty[t], 1);
+      mbar_init(&ctl.mma_drain[t], 1);
       mbar_init(&ctl.s_full[t], 1);
       mbar_init(&ctl.p_half[t][0], 4);  // one elected arrival per softmax warp
       mbar_init(&ctl.p_half[t][1], 4);
@@ -451,10 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl.o_full[t], 1);
       mbar_init(&ctl.o_empty[t], 4);
     }
-    mbar_init(&ctl.mma_drain, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl.kv_full[s], 1);
-      mbar_init(&ctl.kv_empty[s], 1);
+      mbar_init(&ctl.kv_empty[0][s], 1);
+      mbar_init(&ctl.kv_empty[1][s], 1);
     }
     ctl.abort = 0;
     fence_barrier_init();
@@ -496,7 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_kv = policy_evict_last();
     const uint32_t clc_answer = smem_u32(&ctl.clc_answer);
     uint32_t it = 0;         // ring item: K_j of a unit, then V_j, block after block
-    uint32_t nq = 0;         // Q loads issued
+    uint32_t nq[2] = {0, 0}; // Q_t loads issued
+    // Per ring slot (bit s): which query tiles read the item now in the slot,
+    // and the parity of how many items of the slot each tile has read.  A slot
+    // is reloaded once every tile that read its previous item has released it
+    // (kv_empty[t][slot]); under a causal mask tile 0 skips the unit's last
+    // key block, so it neither reads nor releases that block's items.
+    uint32_t rd0 = 0, rd1 = 0, par0 = 0, par1 = 0;
     uint32_t asked = 0;      // cancellation requests issued
     uint32_t answered = 0;   // ... and their answers read
     bool ok = true;
@@ -514,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x < 0) break;
       const Unit u = decode_unit<CAUSAL>(x, p);
       const int q0 = u.qb * 2 * kBM;
-      const int nkv1 = nkv_tile1(u.qb);
+      const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
       if (p.dynamic) {
         // ask for the next unit now; the answer is read half-way through this one
         fence_proxy_async_smem();
@@ -525,12 +541,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int x_next = -1;
       for (int j = 0; ok && j < nkv1; ++j) {
         for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t slot = it % C::kStages;
-          const uint32_t use = it / C::kStages;
-          ok = mbar_wait(&ctl.kv_empty[slot], (use & 1) ^ 1, abort_flag, p.status,
-                         kStatusTimeoutLoad, p.wait_limit_ns);
+          const uint32_t slot = it % C::kStages, bit = 1u << slot;
+          if (rd0 & bit)
+            ok = mbar_wait(&ctl.kv_empty[0][slot], (par0 & bit) ? 0u : 1u, abort_flag, p.status,
+                           kStatusTimeoutLoad, p.wait_limit_ns);
+          if (ok && (rd1 & bit))
+            ok = mbar_wait(&ctl.kv_empty[1][slot], (par1 & bit) ? 0u : 1u, abort_flag, p.status,
+                           kStatusTimeoutLoad, p.wait_limit_ns);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
+          if (C::kIssuers == 1 || j < nkv0) {  // one issuer releases every item as tile 0
+            rd0 |= bit;
+            par0 ^= bit;
+          } else {
+            rd0 &= ~bit;
+          }
+          if (C::kIssuers == 2) {
+            rd1 |= bit;
+            par1 ^= bit;
+          }
           mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
           if (ET == kE4M3 && kv) {
             // V transposed: one box of 128 keys x 128 rows (d)
@@ -544,18 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++it;
           if (j == 0 && kv == 1) {
-            // Q after K_0 and V_0: the previous unit's last Q K^T frees the
-            // Q tiles while this unit's first K/V are already in flight.
-            ok = mbar_wait(&ctl.q_empty, (nq & 1) ^ 1, abort_flag, p.status, kStatusTimeoutLoad,
-                           p.wait_limit_ns);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            mbar_arrive_expect_tx_warp(&ctl.q_full, 2 * C::kTileBytes);
-            for (int t = 0; t < 2; ++t)
+            // Q_t after K_0 and V_0: the previous unit's last Q_t K^T frees
+            // the tile while this unit's first K/V are already in flight.
+            for (int t = 0; ok && t < 2; ++t) {
+              ok = mbar_wait(&ctl.q_empty[t], (nq[t] & 1) ^ 1, abort_flag, p.status,
+                             kStatusTimeoutLoad, p.wait_limit_ns);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+              mbar_arrive_expect_tx_warp(&ctl.q_full[t], C::kTileBytes);
               for (int cb = 0; cb < C::kColBlocks; ++cb)
-                tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full,
+                tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full[t],
                                  cb * C::kBoxElems, q0 + t * kBM, u.bh, pol_q);
-            ++nq;
+              ++nq[t];
+            }
+            if (!ok) break;
           }
           if (p.dynamic && j == nkv1 / 2 && kv == 1) {
             ok = mbar_wait(&ctl.clc_bar, answered & 1, abort_flag, p.status, kStatusTimeoutLoad,
@@ -580,22 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (asked > answered)
       mbar_wait(&ctl.clc_bar, answered & 1, nullptr, p.status, kStatusTimeoutDrain,
                 p.wait_limit_ns);
-    if (nq > 0)
-      mbar_wait(&ctl.q_full, (nq - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
-                p.wait_limit_ns);
+    for (int t = 0; t < 2; ++t)
+      if (nq[t] > 0)
+        mbar_wait(&ctl.q_full[t], (nq[t] - 1) & 1, nullptr, p.status, kStatusTimeoutDrain,
+                  p.wait_limit_ns);
     const uint32_t first = it > (uint32_t)C::kStages ? it - C::kStages : 0u;
     for (uint32_t i = first; i < it; ++i)
       mbar_wait(&ctl.kv_full[i % C::kStages], (i / C::kStages) & 1, nullptr, p.status,
                 kStatusTimeoutDrain, p.wait_limit_ns);
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ================================================================ MMA issuer
-    // The whole warp runs the loop with warp-uniform operands; one elected
-    // lane issues every tcgen05.mma and tcgen05.commit.
-    const uint32_t tS0 = tmem, tS1 = tmem + kBM;
-    const uint32_t tO0 = tmem + C::kOCol, tO1 = tmem + C::kOCol + D;
-    const uint32_t q0_lo = sdesc_lo(sQ, kLboKMajor);
-    const uint32_t q1_lo = sdesc_lo(sQ + C::kTileBytes, kLboKMajor);
+  } else if (warp == kWarpMma || (C::kIssuers == 2 && warp == kWarpMma1)) {
+    // ================================================================ MMA issuers
+    // Each issuer warp runs its loop with warp-uniform operands; one elected
+    // lane issues every tcgen05.mma and tcgen05.commit.  A commit tracks only
+    // the issuing warp's own MMAs: an issuer releases ring slots through
+    // kv_empty[i] (i = its index) and the Q tiles of its query tiles through
+    // q_empty[t].
+    const int issuer = warp == kWarpMma ? 0 : 1;
     auto slot_addr = [&](uint32_t item) { return sRing + (item % C::kStages) * C::kSlotBytes; };
     auto k_lo = [&](uint32_t item) { return sdesc_lo(slot_addr(item), kLboKMajor); };
     auto v_lo = [&](uint32_t item) {
@@ -604,93 +636,107 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       const bool good =
           mbar_wait(bar, parity, abort_flag, p.status, kStatusTimeoutMma, p.wait_limit_ns);
-      return __all_sync(0xffffffffu, good);
+      return __all_sync(0xffffffffu, good) != 0;
     };
     auto wait_full = [&](uint32_t item) {
       return wait(&ctl.kv_full[item % C::kStages], (item / C::kStages) & 1);
     };
+    auto release = [&](uint32_t item) {
+      mma_commit_warp(&ctl.kv_empty[issuer][item % C::kStages]);
+    };
     // O_t += P_t V in two key halves, each as soon as its P is in TMEM; the
     // first half's completion is committed for a softmax that has to rescale
-    // O_t while computing the second half.  g = the tile's block count over
+    // O_t while computing the second half.  gj = the tile's block count over
     // all units of this block (P phases).
-    auto pv_halves = [&](int t, uint32_t tO, uint32_t tP, uint32_t vlo, uint32_t g, int j) {
-      if (!wait(&ctl.p_half[t][0], g & 1)) return false;
+    auto pv_halves = [&](int t, uint32_t tO, uint32_t tP, uint32_t vlo, uint32_t gj, int j) {
+      if (!wait(&ctl.p_half[t][0], gj & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, ET>(tO, tP, vlo, 0, j > 0);
       mma_commit_warp(&ctl.pva_done[t]);
-      if (!wait(&ctl.p_half[t][1], g & 1)) return false;
+      if (!wait(&ctl.p_half[t][1], gj & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, ET>(tO, tP, vlo, 1, true);
       if constexpr (C::kSplitP) mma_commit_warp(&ctl.pvb_done[t]);
       return true;
     };
     bool ok = true;
-    uint32_t it = 0;          // ring item of the unit's K_0
-    uint32_t g0 = 0, g1 = 0;  // key blocks done by tile 0 / tile 1
-    for (uint32_t k = 0; ok; ++k) {
-      int x;
-      ok = next_unit(k, kStatusTimeoutMma, &x);
-      if (!ok || x < 0) break;
-      const Unit u = decode_unit<CAUSAL>(x, p);
-      const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
-      ok = wait_full(it) && wait(&ctl.q_full, k & 1);
-      if (!ok) break;
-      if constexpr (C::kSplitP) {
-        // Split P: Q K^T of tile t waits only until the softmax has read the
-        // previous S_t, so a tile's next S is computed while its softmax still
-        // works on the current block.  Per block j the issue order is
-        // S_0(j+1), P_0 V_j, S_1(j+1), P_1 V_j: each tile's P V is issued as
-        // soon as its P is in TMEM, never behind a wait on the other tile.
-        const uint32_t tP0 = tmem + C::kPCol, tP1 = tmem + C::kPCol + 64;
-        ok = (g0 == 0 || wait(&ctl.s_free[0], (g0 - 1) & 1));
-        if (!ok) break;
+    uint32_t it = 0;  // ring item of the unit's K_0
+    if constexpr (C::kIssuers == 2) {
+      // One issuer per query tile (split P).
+      const int t = issuer;
+      const uint32_t tS = tmem + t * kBM;
+      const uint32_t tO = tmem + C::kOCol + t * D;
+      const uint32_t tP = tmem + C::kPCol + t * 64;
+      const uint32_t q_lo = sdesc_lo(sQ + t * C::kTileBytes, kLboKMajor);
+      // S_t = Q_t K^T of ring item ik; after the unit's last one, Q_t is free.
+      auto qk = [&](uint32_t ik, bool last) {
         tc_fence_after();
-        issue_qk<D, ET>(tS0, q0_lo, k_lo(it));
-        mma_commit_warp(&ctl.s_full[0]);
-        ok = (g1 == 0 || wait(&ctl.s_free[1], (g1 - 1) & 1));
+        issue_qk<D, ET>(tS, q_lo, k_lo(ik));
+        mma_commit_warp(&ctl.s_full[t]);
+        release(ik);
+        if (last) mma_commit_warp(&ctl.q_empty[t]);
+      };
+      uint32_t g = 0;  // key blocks done by this tile over all units of the block
+      for (uint32_t k = 0; ok; ++k) {
+        int x;
+        ok = next_unit(k, kStatusTimeoutMma, &x);
+        if (!ok || x < 0) break;
+        const Unit u = decode_unit<CAUSAL>(x, p);
+        const int nkv = t ? nkv_tile1(u.qb) : nkv_tile0(u.qb);
+        const int nkv1 = nkv_tile1(u.qb);  // the unit's key blocks (ring items / 2)
+        // S_t is overwritten only after the softmax has read it
+        ok = wait_full(it) && wait(&ctl.q_full[t], k & 1) &&
+             (g == 0 || wait(&ctl.s_free[t], (g - 1) & 1));
         if (!ok) break;
-        tc_fence_after();
-        issue_qk<D, ET>(tS1, q1_lo, k_lo(it));
-        mma_commit_warp(&ctl.s_full[1]);
-        mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
-        if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
-        ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
-        for (int j = 0; ok && j < nkv1; ++j) {
+        qk(it, nkv == 1);
+        // The unit's first P V overwrites O_t: the previous unit's epilogue
+        // must have read it.
+        ok = wait(&ctl.o_empty[t], (k & 1) ^ 1);
+        for (int j = 0; ok && j < nkv; ++j) {
           const uint32_t iv = it + 2 * j + 1, ik = it + 2 * j + 2;
-          if (j + 1 < nkv0) {
-            ok = wait_full(ik) && wait(&ctl.s_free[0], (g0 + j) & 1);
+          // The next S_t waits only until the softmax has read this one, so
+          // it is computed while the softmax still works on block j.
+          if (j + 1 < nkv) {
+            ok = wait_full(ik) && wait(&ctl.s_free[t], (g + j) & 1);
             if (!ok) break;
-            tc_fence_after();
-            issue_qk<D, ET>(tS0, q0_lo, k_lo(ik));
-            mma_commit_warp(&ctl.s_full[0]);
+            qk(ik, j + 2 == nkv);
           }
-          ok = wait_full(iv);
-          if (ok && j < nkv0) {
-            ok = pv_halves(0, tO0, tP0, v_lo(iv), g0 + j, j);
-            if (ok && j == nkv0 - 1) mma_commit_warp(&ctl.o_full[0]);
-          }
-          if (ok && j + 1 < nkv1) {
-            ok = wait_full(ik) && wait(&ctl.s_free[1], (g1 + j) & 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk<D, ET>(tS1, q1_lo, k_lo(ik));
-            mma_commit_warp(&ctl.s_full[1]);
-            mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
-            if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
-          }
-          ok = ok && pv_halves(1, tO1, tP1, v_lo(iv), g1 + j, j);
+          ok = wait_full(iv) && pv_halves(t, tO, tP, v_lo(iv), g + j, j);
           if (!ok) break;
-          mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
-          if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
+          release(iv);
+          if (j == nkv - 1) mma_commit_warp(&ctl.o_full[t]);
         }
-      } else {
+        it += 2 * nkv1;
+        g += nkv;
+      }
+    } else {
+      // One issuer for both tiles (P lies over S).  Per block j the issue
+      // order is P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): each S_t(j+1) follows
+      // the P_t V(j) that reads P_t, and the tiles stay half a period apart.
+      const uint32_t tS0 = tmem, tS1 = tmem + kBM;
+      const uint32_t tO0 = tmem + C::kOCol, tO1 = tmem + C::kOCol + D;
+      const uint32_t q0_lo = sdesc_lo(sQ, kLboKMajor);
+      const uint32_t q1_lo = sdesc_lo(sQ + C::kTileBytes, kLboKMajor);
+      auto free_q = [&]() {  // after the unit's last Q K^T (which is tile 1's)
+        mma_commit_warp(&ctl.q_empty[0]);
+        mma_commit_warp(&ctl.q_empty[1]);
+      };
+      uint32_t g0 = 0, g1 = 0;  // key blocks done by tile 0 / tile 1
+      for (uint32_t k = 0; ok; ++k) {
+        int x;
+        ok = next_unit(k, kStatusTimeoutMma, &x);
+        if (!ok || x < 0) break;
+        const Unit u = decode_unit<CAUSAL>(x, p);
+        const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
+        ok = wait_full(it) && wait(&ctl.q_full[0], k & 1) && wait(&ctl.q_full[1], k & 1);
+        if (!ok) break;
         tc_fence_after();
         issue_qk<D, ET>(tS0, q0_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[0]);
         issue_qk<D, ET>(tS1, q1_lo, k_lo(it));
         mma_commit_warp(&ctl.s_full[1]);
-        mma_commit_warp(&ctl.kv_empty[it % C::kStages]);
-        if (nkv1 == 1) mma_commit_warp(&ctl.q_empty);
+        release(it);
+        if (nkv1 == 1) free_q();
         // The unit's first P V overwrites O_0 and O_1: the previous unit's
         // epilogue must have read them (waited here, outside the block loop).
         ok = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
@@ -712,23 +758,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ok = ok && pv_halves(1, tO1, tS1, v_lo(iv), g1 + j, j);
           if (!ok) break;
-          mma_commit_warp(&ctl.kv_empty[iv % C::kStages]);
+          release(iv);
           if (j == nkv1 - 1) mma_commit_warp(&ctl.o_full[1]);
           if (more) {
             issue_qk<D, ET>(tS1, q1_lo, k_lo(ik));
             mma_commit_warp(&ctl.s_full[1]);
-            mma_commit_warp(&ctl.kv_empty[ik % C::kStages]);
-            if (j + 2 == nkv1) mma_commit_warp(&ctl.q_empty);  // the unit's last Q K^T
+            release(ik);
+            if (j + 2 == nkv1) free_q();
           }
         }
+        it += 2 * nkv1;
+        g0 += nkv0;
+        g1 += nkv1;
       }
-      it += 2 * nkv1;
-      g0 += nkv0;
-      g1 += nkv1;
     }
     // Drain: all issued MMAs complete before TMEM can be released.
-    mma_commit_warp(&ctl.mma_drain);
-    mbar_wait(&ctl.mma_drain, 0, nullptr, p.status, kStatusTimeoutDrain, p.wait_limit_ns);
+    mma_commit_warp(&ctl.mma_drain[issuer]);
+    mbar_wait(&ctl.mma_drain[issuer], 0, nullptr, p.status, kStatusTimeoutDrain,
+              p.wait_limit_ns);
     __syncwarp();
   } else {
     // ================================================================ softmax tile t
@@ -1011,7 +1058,7 @@ static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+  kern<<<grid, Cfg<D, ET>::kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
   return cudaGetLastError();
 }
 
