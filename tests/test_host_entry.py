@@ -83,3 +83,23 @@ def test_bwd_host_entry_matches_device_entry(shape, causal, dtype, chunks):
     diff = (dq_h.float() - dq_r.float()).abs()
     lim = ulp * dq_r.float().abs() + 1e-5 * float(dq_r.float().abs().max())
     assert bool((diff <= lim).all()), "dQ differs by %.3e" % float(diff.max())
+
+
+def test_host_entry_e4m3_matches_device_entry():
+    """The host-buffer entry with E4M3 inputs (V transposed per head, O bf16):
+    bit-identical to fmha_fwd on the same staged tensors."""
+    w = synthetic.Workload("host-e4m3", 2, 3, 512, 128, "e4m3", True, 1.0, 88)
+    q, k, v = synthetic.make_inputs(w)
+    vt = synthetic.kernel_v(v)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, vt))
+    ho = torch.full(q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    hl = torch.full(q.shape[:3], float("nan"), dtype=torch.float32).pin_memory()
+    q_dev, k_dev, v_dev = (torch.empty_like(t, device="cuda") for t in (q, k, vt))
+    o_dev = torch.empty(q.shape, dtype=torch.bfloat16, device="cuda")
+    lse_dev = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    wsa.fmha_fwd_host(hq, hk, hv, ho, hl, q_dev, k_dev, v_dev, o_dev, lse_dev, causal=True,
+                      scale=w.scale, n_chunks=3)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    o_ref, l_ref = wsa.attention(q.cuda(), k.cuda(), vt.cuda(), causal=True, scale=w.scale)
+    assert wsa.get_device_status() == wsa.FMHA_OK
+    assert torch.equal(ho, o_ref.cpu()) and torch.equal(hl, l_ref.cpu())
