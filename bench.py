@@ -68,7 +68,7 @@ import synthetic  # noqa: E402
 METRIC = "FMHA fwd TFLOPS at B4 H32 S16K D128 fp16; % of GB300 dense tensor peak"
 UNIT = "TFLOPS"
 KERNEL_SOURCES = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu",
-                  "fmha_fwd_e4m3.cu", "fmha_api.cu"]
+                  "fmha_fwd_e4m3.cu", "fmha_fwd_ksplit.cu", "fmha_api.cu"]
 BWD_SOURCES = ["fmha_bwd_sm103.cuh", "fmha_bwd.cu"]
 TOL_O, TOL_LSE = 1e-2, 1e-3       # the forward parity bar for 16-bit inputs
 

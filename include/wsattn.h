@@ -90,6 +90,12 @@ typedef enum { FMHA_F16 = 0, FMHA_BF16 = 1, FMHA_E4M3 = 2 } fmha_dtype;
  * several host threads on different streams; note that the timeout status is
  * one word per device, shared by every stream and thread (see
  * fmha_get_device_status).
+ *
+ * Results are deterministic for a given shape on a given GPU model.  With full
+ * attention, D = 128 and an even ceil(S/128), the units of a short last wave
+ * (at most half the multiprocessors' worth) are computed in two key halves
+ * and merged, so the rounding of those rows depends on the multiprocessor
+ * count; every result stays within the same bounds of the exact one.
  */
 fmha_status fmha_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,

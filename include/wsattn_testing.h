@@ -1,12 +1,13 @@
 /*
  * wsattn_testing.h -- test hooks of libwsattn.so.  Not for production callers.
  *
- * The pages have no counterpart: this entry point exists so that two properties
- * of the kernel can be tested.  (1) Its bounded waits: every mbarrier wait gives
- * up after a time limit, raises an abort flag for the block, drains in-flight
- * copies and MMAs, frees Tensor Memory and records a status bit -- exercised
- * here without faulting a GPU.  (2) The independence of the result from the
- * online softmax's lazy-rescale threshold.
+ * The pages have no counterpart: these entry points exist so that three
+ * properties of the kernel can be tested.  (1) Its bounded waits: every
+ * mbarrier wait gives up after a time limit, raises an abort flag for the
+ * block, drains in-flight copies and MMAs, frees Tensor Memory and records a
+ * status bit -- exercised here without faulting a GPU.  (2) The independence
+ * of the result from the online softmax's lazy-rescale threshold.  (3) The
+ * key-split units of a short last wave, in every mix with whole units.
  */
 #ifndef WSATTN_TESTING_H_
 #define WSATTN_TESTING_H_
@@ -43,6 +44,29 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
                              int64_t B, int64_t H, int64_t S, int64_t D, int causal, float scale,
                              fmha_dtype dtype, void* stream, int inject_fault,
                              double wait_limit_s, float tau);
+
+/*
+ * fmha_fwd_split_testing -- fmha_fwd with the number of key-split units given.
+ *
+ * Full attention runs on persistent blocks that take (head, 256-row query
+ * block) units in index order.  fmha_fwd splits the units of a short last
+ * wave: the last split_units units each run as two 128-row halves whose two
+ * query tiles take half of the key blocks each, merged in the block
+ * (O = sum of each half's O weighted by its share of the softmax sum).  This
+ * hook fixes that number, so that tests can compare every mix with the
+ * oracle.
+ *
+ *   split_units  -1: as fmha_fwd.  0: none.  1 .. units: the last split_units
+ *                units (units = B * H * ceil(S / 256)).  A positive value
+ *                needs causal = 0, D = 128 and an even ceil(S / 128), else
+ *                FMHA_ERR_UNSUPPORTED; above units is FMHA_ERR_INVALID_ARG.
+ *
+ * Other arguments, ownership and errors as fmha_fwd.
+ */
+fmha_status fmha_fwd_split_testing(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                   int causal, float scale, fmha_dtype dtype, void* stream,
+                                   int64_t split_units);
 
 #ifdef __cplusplus
 }

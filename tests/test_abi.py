@@ -145,6 +145,27 @@ def test_testing_hook_rejects_bad_knobs(lib):
     assert lib.fmha_fwd_testing(*args8, 0, 1.0, 8.5) == wsa.FMHA_ERR_INVALID_ARG
 
 
+def test_split_hook_rejects_unsupported_splits(lib):
+    """Key-split units need full attention, head dim 128 and an even number of
+    key blocks; the count is checked against the units before any CUDA call."""
+    q, k, v, o, lse = _ptrs()
+    def call(S=1024, D=128, causal=0, split=1, B=1, H=2):
+        return lib.fmha_fwd_split_testing(q, k, v, o, lse, B, H, S, D, causal, 0.088, 0, None,
+                                          split)
+    assert call(split=-2) == wsa.FMHA_ERR_INVALID_ARG
+    assert call(causal=1) == wsa.FMHA_ERR_UNSUPPORTED
+    assert call(D=64) == wsa.FMHA_ERR_UNSUPPORTED
+    assert call(S=1152) == wsa.FMHA_ERR_UNSUPPORTED       # 9 key blocks
+    assert call(S=128) == wsa.FMHA_ERR_UNSUPPORTED        # 1 key block
+    assert call(split=9) == wsa.FMHA_ERR_INVALID_ARG      # 8 units (2 heads x 4)
+    assert call(S=0) == wsa.FMHA_ERR_INVALID_ARG
+    # 0 and -1 (none, automatic) go on to fmha_fwd's own checks
+    assert lib.fmha_fwd_split_testing(0, k, v, o, lse, 1, 2, 1024, 128, 0, 0.088, 0, None,
+                                      0) == wsa.FMHA_ERR_INVALID_ARG
+    assert lib.fmha_fwd_split_testing(0, k, v, o, lse, 1, 2, 1024, 128, 0, 0.088, 0, None,
+                                      -1) == wsa.FMHA_ERR_INVALID_ARG
+
+
 def test_e4m3_overlap_uses_the_byte_sizes(lib):
     """Inputs are 1 byte per element and O 2 bytes: an O that starts inside
     the second half of a same-count 16-bit-sized region of q is still past q's

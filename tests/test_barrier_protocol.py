@@ -25,7 +25,11 @@ warp_specialized_attention_gb300/csrc/fmha_fwd_sm103.cuh:
              s_free, pva_done/pvb_done): one issuer per query tile, each
              releasing the ring items and the Q tile its tile read
   softmax    4 warps per query tile: S wait, P releases in two halves, the
-             rescale waits, epilogue (o_full/o_empty)
+             rescale waits, epilogue (o_full/o_empty); in a key-split unit
+             (both tiles on the same 128 query rows, tile 0 on the first half
+             of the keys, tile 1 on the second) tile 1 hands its row
+             statistics over (merge) and tile 0 writes the merged result and
+             frees both O tiles
   tensor     each issuer's commits complete in its own issue order after
              random delays; two issuers' commits interleave freely
   TMA        copies complete in any order after random delays
@@ -57,9 +61,11 @@ class Bar:
 class Model:
     def __init__(self, units, split, stages, seed, causal):
         self.rng = random.Random(seed)
-        self.units = units           # list of (nkv0, nkv1)
+        self.units = [u if len(u) == 3 else (u[0], u[1], False) for u in units]
+        # (nkv0, nkv1, key_split): a key-split unit has nkv0 == nkv1 blocks per tile
         self.split = split
         self.stages = stages
+        self.merge_every_unit = not split and not causal   # the kernels that may key-split
         self.errors = []
         self.bars = {}
         self.tma_q = []              # pending copies, completed in any order
@@ -68,6 +74,7 @@ class Model:
         for i in range(2):
             b(("unit_full", i), 1)
             b(("unit_empty", i), 10 if split else 9)   # issuers + eight softmax warps
+        b(("merge",), 4)                                 # tile 1's warps, key-split units
         for t in range(2):
             for n, c in (("s_full", 1), ("p0", 4), ("p1", 4), ("pva", 1), ("pvb", 1),
                          ("s_free", 4), ("o_full", 1), ("o_empty", 4), ("q_full", 1),
@@ -79,6 +86,7 @@ class Model:
                 b(("kv_empty", t, s), 1)
         self.unit_slot = [None, None]
         self.slot_item = [None] * stages   # which ring item each slot holds (set when a copy lands)
+        self.stats = [None] * 4            # per warp quadrant: whose row statistics tile 1 left
 
     def bar(self, name, count):
         self.bars[name] = Bar(count)
@@ -118,9 +126,10 @@ class Model:
             self.bars[("unit_full", k & 1)].arrive()
             if k == len(self.units):
                 return
-            n0, n1 = self.units[k]
+            n0, n1, ks = self.units[k]
             for j in range(n1):
-                for kv in range(2):
+                # a key-split unit loads K_j, K_{h+j}, V_j, V_{h+j} per step
+                for kv in range(4 if ks else 2):
                     slot = it % self.stages
                     for t in range(2):
                         if mask[slot] >> t & 1:
@@ -132,7 +141,7 @@ class Model:
                         uses[t][slot] += mask[slot] >> t & 1
                     self.copy(("kv_full", slot), it)
                     it += 1
-                    if j == 0 and kv == 1:
+                    if j == 0 and kv == (3 if ks else 1):
                         for t in range(2):
                             if nq[t] > 0:
                                 yield from self.wait(("q_empty", t), nq[t] - 1)
@@ -208,9 +217,11 @@ class Model:
             u = yield from self.next_unit(k)
             if u < 0:
                 return
-            n0, n1 = self.units[u]
-            K = lambda j: it + 2 * j
-            V = lambda j: it + 2 * j + 1
+            n0, n1, ks = self.units[u]
+            # ring items: both tiles read K_j, V_j; a key-split unit gives each
+            # tile its own K and V per step (tile 1 on keys h + j)
+            K = lambda t, j: it + 4 * j + t if ks else it + 2 * j
+            V = lambda t, j: it + 4 * j + 2 + t if ks else it + 2 * j + 1
             full = lambda item: self.wait(("kv_full", item % self.stages), item // self.stages)
             release = lambda item: self.commit(0, ("release", 0, item))
 
@@ -227,12 +238,16 @@ class Model:
                 self.commit(0, ("q_empty", 0))
                 self.commit(0, ("q_empty", 1))
 
-            yield from use(K(0))
+            yield from use(K(0, 0))
+            if ks:
+                yield from use(K(1, 0))
             yield from self.wait(("q_full", 0), k)
             yield from self.wait(("q_full", 1), k)
             self.commit(0, ("s_full", 0))
             self.commit(0, ("s_full", 1))
-            release(K(0))
+            release(K(0, 0))
+            if ks:
+                release(K(1, 0))
             if n1 == 1:
                 free_q()
             if k > 0:
@@ -240,30 +255,39 @@ class Model:
                 yield from self.wait(("o_empty", 1), k - 1)
             for j in range(n1):
                 more = j + 1 < n1
-                yield from use(V(j))
+                yield from use(V(0, j))
                 if j < n0:
                     yield from pv(0, g0, j)
                     if j == n0 - 1:
                         self.commit(0, ("o_full", 0))
+                if ks:
+                    release(V(0, j))
                 if more:
-                    yield from use(K(j + 1))
+                    yield from use(K(0, j + 1))
                     if j + 1 < n0:
                         self.commit(0, ("s_full", 0))
+                    if ks:
+                        release(K(0, j + 1))
+                if ks:
+                    yield from use(V(1, j))
                 yield from pv(1, g1, j)
-                release(V(j))
+                release(V(1, j))
                 if j == n1 - 1:
                     self.commit(0, ("o_full", 1))
                 if more:
+                    if ks:
+                        yield from use(K(1, j + 1))
                     self.commit(0, ("s_full", 1))
-                    release(K(j + 1))
+                    release(K(1, j + 1))
                     if j + 2 == n1:
                         free_q()
-            it += 2 * n1
+            it += 2 * (n0 + n1) if ks else 2 * n1
             g0 += n0
             g1 += n1
             k += 1
 
-    def softmax(self, t):
+    def softmax(self, t, q):
+        """Softmax warp q (TMEM lane quadrant q) of query tile t."""
         g = 0
         k = 0
         rng = self.rng
@@ -272,6 +296,7 @@ class Model:
             if u < 0:
                 return
             nkv = self.units[u][t]
+            ks = self.units[u][2]
             for j in range(nkv):
                 gj = g + j
                 yield from self.wait(("s_full", t), gj)
@@ -293,7 +318,21 @@ class Model:
                 self.bars[("p1", t)].arrive()
             g += nkv
             yield from self.wait(("o_full", t), k)
-            self.bars[("o_empty", t)].arrive()
+            if t == 1 and self.merge_every_unit:
+                # tile 1 arrives in every unit: phase k of the barrier is unit k's
+                if ks:
+                    self.stats[q] = u                # row statistics handed to tile 0
+                self.bars[("merge",)].arrive()
+            if not ks:
+                self.bars[("o_empty", t)].arrive()
+            elif t == 0:
+                yield from self.wait(("o_full", 1), k)
+                yield from self.wait(("merge",), k)
+                if self.stats[q] != u:
+                    self.errors.append("tile 0 merged unit %d with statistics of unit %s"
+                                       % (u, self.stats[q]))
+                self.bars[("o_empty", 0)].arrive()   # both O tiles read: free them
+                self.bars[("o_empty", 1)].arrive()
             k += 1
 
     def engines(self):
@@ -319,7 +358,7 @@ class Model:
 
     def run(self, max_idle=20000):
         issuers = [self.mma_tile(0), self.mma_tile(1)] if self.split else [self.mma_single()]
-        roles = [self.producer()] + issuers + [self.softmax(t) for t in range(2) for _ in range(4)]
+        roles = [self.producer()] + issuers + [self.softmax(t, q) for t in range(2) for q in range(4)]
         engines = self.engines()
         alive = list(roles)
         idle = 0
@@ -344,11 +383,17 @@ class Model:
         return "ok"
 
 
-def _units(rng, causal, n_units):
+def _units(rng, causal, n_units, key_split=False):
+    """Random units; with key_split, the tail units (after a random number of
+    whole ones, as the host places them) split the keys between the tiles."""
     out = []
-    for _ in range(n_units):
+    n_whole = rng.randint(0, n_units) if key_split else n_units
+    for i in range(n_units):
         qb = rng.randint(0, 4)
-        out.append((2 * qb + 1, 2 * qb + 2) if causal else (qb + 1, qb + 1))
+        if i >= n_whole:
+            out.append((qb + 1, qb + 1, True))
+        else:
+            out.append((2 * qb + 1, 2 * qb + 2) if causal else (qb + 1, qb + 1))
     return out
 
 
@@ -363,11 +408,40 @@ def test_protocol_has_no_deadlock_and_no_false_pass(split, causal):
         assert res == "ok", "seed %d units %s: %s" % (seed, units, res)
 
 
+def test_protocol_with_key_split_tail_units():
+    """Full attention, head dim 128: whole units followed by key-split ones
+    (each tile on half of the keys of the same 128 query rows, merged in the
+    block)."""
+    for seed in range(400):
+        rng = random.Random(seed)
+        units = _units(rng, False, rng.randint(1, 6), key_split=True)
+        res = Model(units, False, 4, seed, False).run()
+        assert res == "ok", "seed %d units %s: %s" % (seed, units, res)
+
+
+def test_model_detects_a_merge_without_the_other_tile():
+    """Negative control: a tile 0 that frees O_1 without waiting for tile 1's
+    last P V lets the next unit's P V overwrite O_1 while it may still be
+    read; the model must report the false pass or a deadlock."""
+    class NoWait(Model):
+        def wait(self, name, index):
+            if name == ("merge",):
+                return iter(())            # the dropped wait
+            return Model.wait(self, name, index)
+    bad = 0
+    for seed in range(200):
+        rng = random.Random(seed)
+        units = [(2, 2, True)] * rng.randint(2, 4)
+        if NoWait(units, False, 4, seed, False).run() != "ok":
+            bad += 1
+    assert bad > 0
+
+
 def test_model_detects_a_deadlock():
     """Negative control: a softmax that waits for the P V of the keys it has
     not released yet (its own second half) must be reported as a deadlock."""
     class SelfWait(Model):
-        def softmax(self, t):
+        def softmax(self, t, q):
             u = yield from self.next_unit(0)
             yield from self.wait(("s_full", t), 0)
             self.bars[("p0", t)].arrive()

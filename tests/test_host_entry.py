@@ -1,6 +1,7 @@
 """fmha_fwd_host: host-resident tensors, transfers overlapped with compute in
 chunks of (batch, head) slices.  Rows of different slices are independent, so
-the outputs must be bit-identical to fmha_fwd on the same staged inputs."""
+the outputs must be bit-identical to fmha_fwd on the same staged inputs (the
+chunks key-split the units that fmha_fwd splits on the whole problem)."""
 import pytest
 import torch
 
@@ -15,6 +16,9 @@ pytestmark = pytest.mark.gpu
     ((2, 3, 384, 128), True, torch.bfloat16, 4),
     ((1, 5, 300, 64), True, torch.float16, 1),
     ((1, 2, 256, 64), False, torch.float16, 64),   # more chunks than slices
+    ((2, 3, 512, 128), False, torch.float16, 4),    # every unit key-split
+    ((1, 40, 1024, 128), False, torch.bfloat16, 3),  # the last units key-split (152 SMs)
+    ((1, 40, 1024, 128), False, torch.float16, 0),
 ])
 def test_host_entry_matches_device_entry(shape, causal, dtype, chunks):
     B, H, S, D = shape

@@ -25,7 +25,8 @@ import torch
 __all__ = [
     "FMHA_OK", "FMHA_ERR_INVALID_ARG", "FMHA_ERR_UNSUPPORTED", "FMHA_ERR_CUDA",
     "FMHA_ERR_TIMEOUT", "FMHA_F16", "FMHA_BF16", "FMHA_E4M3", "FmhaError", "LibraryNotBuilt",
-    "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing", "attention",
+    "library_path", "load_library", "fmha_fwd", "fmha_fwd_host", "fmha_fwd_testing",
+    "fmha_fwd_split_testing", "attention",
     "fmha_bwd", "fmha_bwd_workspace_bytes", "fmha_bwd_noalloc", "fmha_bwd_host",
     "fmha_bwd_host_scratch_bytes", "attention_backward", "AttentionFunction",
     "flash_attention",
@@ -79,6 +80,8 @@ def load_library():
         lib.fmha_fwd_host.restype = ctypes.c_int
         lib.fmha_fwd_testing.argtypes = fwd_args + [ctypes.c_int, ctypes.c_double, ctypes.c_float]
         lib.fmha_fwd_testing.restype = ctypes.c_int
+        lib.fmha_fwd_split_testing.argtypes = fwd_args + [i64]
+        lib.fmha_fwd_split_testing.restype = ctypes.c_int
         lib.fmha_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.fmha_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fmha_bwd.argtypes = [vp] * 10 + [ctypes.c_size_t, i64, i64, i64, i64, ctypes.c_int,
@@ -221,6 +224,20 @@ def fmha_fwd_testing(q, k, v, o, lse, causal: bool, scale: float, inject_fault: 
                                         lse.data_ptr(), B, H, S, D, int(bool(causal)),
                                         float(scale), _dtype_code(q), _stream_handle(stream),
                                         int(inject_fault), float(wait_limit_s), float(tau)))
+
+
+def fmha_fwd_split_testing(q, k, v, o, lse, causal: bool, scale: float, split_units: int,
+                           stream=None) -> int:
+    """Test hook of include/wsattn_testing.h (the number of key-split units
+    of the last wave); returns the raw status code."""
+    lib = load_library()
+    _check(q, k, v, o, lse)
+    B, H, S, D = q.shape
+    with torch.cuda.device(q.device):
+        return int(lib.fmha_fwd_split_testing(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              o.data_ptr(), lse.data_ptr(), B, H, S, D,
+                                              int(bool(causal)), float(scale), _dtype_code(q),
+                                              _stream_handle(stream), int(split_units)))
 
 
 def get_device_status(stream=None, device=None) -> int:

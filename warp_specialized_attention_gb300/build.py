@@ -28,7 +28,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v
          "-I" + INCLUDE, "-I" + CSRC]
 
 LIB_UNITS = ["fmha_api.cu", "fmha_fwd_d64.cu", "fmha_fwd_d128.cu", "fmha_fwd_e4m3.cu",
-             "fmha_bwd.cu"]
+             "fmha_fwd_ksplit.cu", "fmha_bwd.cu"]
 PROBE_UNITS = ["probes.cu"]
 HEADERS = ["ptx.cuh", "fmha_fwd_sm103.cuh", "fmha_bwd_sm103.cuh", "fmha_launch.h"]
 

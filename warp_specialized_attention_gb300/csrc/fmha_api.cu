@@ -168,6 +168,40 @@ int causal_group_heads(int64_t BH, int64_t S, int64_t D) {
   return static_cast<int>((BH + groups - 1) / groups);
 }
 
+// Streaming multiprocessors of the current device, looked up once per device.
+cudaError_t sm_count(int* out) {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable && (*out = cache[dev].load(std::memory_order_acquire)) > 0) return cudaSuccess;
+  e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && cacheable) cache[dev].store(*out, std::memory_order_release);
+  return e;
+}
+
+// Whether units of this shape may be key-split: full attention under the
+// one-issuer schedule (head dim 128), and an even number of key blocks, so
+// that each tile of a split unit takes the same number of whole blocks and
+// every tile's keys include at least one unmasked key.
+bool key_split_allowed(int64_t S, int64_t D, int causal) {
+  const int64_t nkv = (S + 127) / 128;
+  return !causal && D == 128 && nkv % 2 == 0;
+}
+
+// How many of the last units to key-split.  Every full-attention unit costs
+// the same, so with U units on n_sm SMs (one block each) the last wave holds
+// U mod n_sm units and leaves the other SMs idle.  When that remainder fits
+// in half of the SMs, its units are split: each becomes two 128-row halves
+// whose two tiles take half of the keys each, so the last wave takes about
+// half as long (B4 H32 S1K: 512 units, the last 56 on 152 SMs).
+int64_t auto_split_units(int64_t units, int64_t S, int64_t D, int causal, int n_sm) {
+  if (!key_split_allowed(S, D, causal) || n_sm <= 0) return 0;
+  const int64_t r = units % n_sm;
+  return 2 * r <= n_sm ? r : 0;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -208,7 +242,8 @@ fmha_status validate(const void* q, const void* k, const void* v, void* o, float
 
 fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t S, int64_t D, int causal, float scale, int dtype,
-                     void* stream, int inject, uint64_t wait_limit_ns, float tau = -1.f) {
+                     void* stream, int inject, uint64_t wait_limit_ns, float tau = -1.f,
+                     int64_t split_units = -1) {
   const fmha_status vs = validate(q, k, v, o, lse, B, H, S, D, scale, dtype);
   if (vs != FMHA_OK) return vs;
 
@@ -251,12 +286,24 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   prm.tau = tau;
   prm.p_shift = e4m3 ? 8.f - tau : 0.f;
   prm.two_pow_tau = std::exp2(tau + prm.p_shift);
-  const unsigned grid = static_cast<unsigned>(prm.n_qblk * BH);
+  // The last split_units units run as key-split halves: two grid blocks each.
+  const int64_t units = prm.n_qblk * BH;
+  if (split_units < 0) {
+    int n_sm = 0;
+    e = sm_count(&n_sm);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
+    split_units = auto_split_units(units, S, D, causal, n_sm);
+  }
+  if (units + split_units > (int64_t{1} << 31) - 1) split_units = 0;
+  prm.n_whole = static_cast<int>(units - split_units);
+  const unsigned grid = static_cast<unsigned>(units + split_units);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  e = e4m3      ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, to, prm, grid, st)
-      : D == 64 ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, to, prm, grid, st)
-                : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, to, prm, grid, st);
+  e = split_units > 0 ? wsa::launch_fwd_ksplit(e4m3 ? wsa::kE4M3 : bf16 ? wsa::kBF16 : wsa::kF16,
+                                               tq, tk, tv, to, prm, grid, st)
+      : e4m3          ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, to, prm, grid, st)
+      : D == 64       ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, to, prm, grid, st)
+                      : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, to, prm, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return FMHA_OK;
 }
@@ -440,6 +487,14 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
   auto at = [](const void* p, size_t off) {
     return static_cast<void*>(static_cast<char*>(const_cast<void*>(p)) + off);
   };
+  // The units that fmha_fwd would key-split on the whole problem (its last
+  // ones) are key-split in the chunks that hold them, so that the result is
+  // the same bits as fmha_fwd's.
+  const int64_t nq = (S + 255) / 256;
+  int n_sm = 0;
+  if ((e = sm_count(&n_sm)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
+  const int64_t first_split = BH * nq - auto_split_units(BH * nq, S, D, causal, n_sm);
   for (int64_t c = 0; c < chunks; ++c) {
     // chunks alternate between two compute streams, so that one chunk's
     // kernel can start on the SMs that the previous one's last wave leaves
@@ -459,10 +514,11 @@ fmha_status fwd_host_impl(const void* q, const void* k, const void* v, void* o, 
         (e = cudaStreamWaitEvent(cs, hp->copied[c], 0)) != cudaSuccess)
       return cuda_fail(e, "host-to-device copy");
     // one (batch, head) range is a B = 1, H = n problem at offset pointers
+    const int64_t split = std::max<int64_t>(0, s1 * nq - std::max(s0 * nq, first_split));
     const fmha_status ks =
         fwd_impl(at(q_dev, off), at(k_dev, off), at(v_dev, off), at(o_dev, ooff),
                  static_cast<float*>(at(lse_dev, loff)), 1, n, S, D, causal, scale, dtype, cs, 0,
-                 kDefaultWaitLimitNs);
+                 kDefaultWaitLimitNs, -1.f, split);
     if (ks != FMHA_OK) return ks;
     if ((e = cudaEventRecord(hp->computed[c], cs)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->d2h, hp->computed[c], 0)) != cudaSuccess ||
@@ -619,6 +675,21 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
   if (!(tau >= 0.f && tau <= (dtype == FMHA_E4M3 ? 8.f : 15.f))) return FMHA_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream,
                   inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9), tau);
+}
+
+fmha_status fmha_fwd_split_testing(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
+                                   int causal, float scale, fmha_dtype dtype, void* stream,
+                                   int64_t split_units) {
+  if (split_units < -1) return FMHA_ERR_INVALID_ARG;
+  if (split_units > 0) {
+    const fmha_status vs = validate_sizes(B, H, S, D, scale, static_cast<int>(dtype));
+    if (vs != FMHA_OK) return vs;
+    if (!key_split_allowed(S, D, causal)) return FMHA_ERR_UNSUPPORTED;
+    if (split_units > ((S + 255) / 256) * B * H) return FMHA_ERR_INVALID_ARG;
+  }
+  return fwd_impl(q, k, v, o, lse, B, H, S, D, causal, scale, static_cast<int>(dtype), stream, 0,
+                  kDefaultWaitLimitNs, -1.f, split_units);
 }
 
 fmha_status fmha_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,

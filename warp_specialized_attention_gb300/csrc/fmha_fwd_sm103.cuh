@@ -42,6 +42,20 @@
 // reloaded once the previous unit's last Q K^T is done (q_full / q_empty) and
 // O_t is overwritten only after the previous epilogue read it (o_empty).
 //
+// Key-split units.  Full-attention units all cost the same, so a last wave of
+// r < #SMs units leaves the other SMs idle for a whole unit.  When r is at most
+// half the SMs, the host makes those units key-split: each becomes two grid
+// blocks (units), one per 128-row half, and within a half tile 0 takes the
+// first h of the 2h key blocks and tile 1 the rest (ring items K_j, K_{h+j},
+// V_j, V_{h+j} per step), so the last wave takes half as long.  Tile 1
+// then leaves its row statistics (m_1, l_1) in shared memory (merge barrier),
+// and tile 0 combines the two tiles: m = max(m_0, m_1), l = l_0 2^(m_0 - m) +
+// l_1 2^(m_1 - m), O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / l -- the online
+// softmax's rescaling applied once more, as when two blocks of keys are
+// combined -- and frees both O tiles.  (The wave quantisation that this
+// shortens is the W of "A Performance Model for Warp Specialization
+// Kernels", core formulas.)
+//
 // Synchronisation is the aref channel of the Tawa page (Section III-B/III-E):
 // every ring slot has a full barrier (TMA transaction bytes) and an empty
 // barrier (arrived by tcgen05.commit when the MMAs that read the slot finish);
@@ -120,15 +134,9 @@ struct Cfg {
   static constexpr int kStageBoxes = ET == kE4M3 ? 2 : 1;
   static constexpr int kStageBoxBytes = 32 * 128;
   static constexpr int kStageOff = kRingOff + kStages * kSlotBytes;
-  static constexpr int kCtlOff = kStageOff + 8 * kStageBoxes * kStageBoxBytes;
-  static constexpr int kSmemBytes = 1024 + kCtlOff + 512;  // + alignment slack + control
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
-  static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
   // D = 64 leaves 128 TMEM columns free: P_t gets its own 64 columns there
   // (split P), so S_t can be overwritten as soon as the softmax has read it.
   static constexpr bool kSplitP = D == 64 && ET != kE4M3;
-  static constexpr uint32_t kPCol = 256 + 2 * D;           // split P_t at kPCol + 64t
-  static_assert(!kSplitP || kPCol + 128 <= 512, "TMEM columns");
   // MMA issuers.  At D = 128 one warp issues both tiles' MMAs in the order
   // P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): that order keeps the two tiles
   // half a block period apart, so one tile's softmax runs while the other
@@ -138,6 +146,17 @@ struct Cfg {
   static constexpr int kIssuers = kSplitP ? 2 : 1;
   static constexpr int kThreads = kIssuers == 2 ? 352 : 320;  // 11 or 10 warps
   static constexpr int kUnitReaders = 8 + kIssuers;           // softmax warps + issuers
+  // Key-split units (full attention, one issuer): both tiles take the same
+  // 128 query rows, tile 0 the first half of the key blocks and tile 1 the
+  // second; tile 1 leaves its row statistics (m, l) in its staging boxes,
+  // which it has no O to store from, for tile 0, which merges the two O tiles.
+  static constexpr bool kKeySplit = kIssuers == 1;
+  static constexpr int kCtlOff = kStageOff + 8 * kStageBoxes * kStageBoxBytes;
+  static constexpr int kSmemBytes = 1024 + kCtlOff + 512;  // + alignment slack + control
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+  static constexpr uint32_t kOCol = 256;                   // O_t at kOCol + t*D
+  static constexpr uint32_t kPCol = 256 + 2 * D;           // split P_t at kPCol + 64t
+  static_assert(!kSplitP || kPCol + 128 <= 512, "TMEM columns");
 };
 
 struct Ctl {
@@ -160,6 +179,8 @@ struct Ctl {
   uint64_t kv_empty[2][8]; // [tile][slot]: that tile's MMAs have finished reading the slot
   uint32_t tmem_base;
   int abort;
+  uint64_t merge;          // key-split instantiations: tile 1 is done with the unit
+                           // (and left its row statistics if the unit is key-split)
 };
 static_assert(sizeof(Ctl) <= 512, "control block size");
 
@@ -170,6 +191,8 @@ struct FwdParams {
   int n_qblk;         // ceil(S / 256)
   int BH;             // B * H
   int group_heads;    // causal unit order: heads per L2 group (>= 1)
+  int n_whole;        // full attention: units x >= n_whole are the 128-row halves
+                      // of key-split units (n_qblk * BH when none is split)
   int dynamic;        // 1: blocks take further units by cluster launch control
   float scale_log2;   // scale * log2(e)
   uint64_t wait_limit_ns;
@@ -182,26 +205,45 @@ struct FwdParams {
                       // factor, so O = P V / l is unchanged)
 };
 
-// A work unit: one (batch*head) index and one 256-row query block.
+// A work unit: one (batch*head) index and one 256-row query block, or, for a
+// key-split unit, one 128-row half of it whose keys the two tiles share out.
 struct Unit {
   int bh;
   int qb;
+  int ks;  // 1: key-split unit
+  int r0;  // first query row of tile 0 (of both tiles when ks)
 };
+
+template <bool KSPLIT>
+__device__ __forceinline__ int tile_row0(const Unit& u, int t) {
+  return KSPLIT ? u.r0 + (u.ks ? 0 : t * kBM) : u.qb * 2 * kBM + t * kBM;
+}
 
 // Unit index -> (head, query block); the grid has one block per unit and the
 // hardware starts (or hands over) blocks in index order, so this fixes the
 // order in which units begin.  Full attention: head-major, every unit costs
-// the same.  Causal: unit qb costs 2qb+1 or 2qb+2 key blocks, so heads are
-// taken in groups whose K and V fit in L2 together and, inside a group, the
-// longest query blocks of all its heads go first (longest-processing-time-first
-// list scheduling) -- the schedule that shortens the tail, without making K/V
-// of a head leave L2 between its units.
-template <bool CAUSAL>
+// the same; the units of the last wave can be split (index n_whole + 2i + h
+// is half h of unit n_whole + i), so that a last wave that would leave most
+// SMs idle takes half as long.  Causal: unit qb costs 2qb+1 or 2qb+2 key
+// blocks, so heads are taken in groups whose K and V fit in L2 together and,
+// inside a group, the longest query blocks of all its heads go first
+// (longest-processing-time-first list scheduling) -- the schedule that
+// shortens the tail, without making K/V of a head leave L2 between its units.
+template <bool CAUSAL, bool KSPLIT>
 __device__ __forceinline__ Unit decode_unit(int x, const FwdParams& p) {
   Unit u;
+  u.ks = 0;
   if (!CAUSAL) {
+    int half = 0;
+    if (KSPLIT && x >= p.n_whole) {
+      const int y = x - p.n_whole;
+      x = p.n_whole + (y >> 1);
+      half = y & 1;
+      u.ks = 1;
+    }
     u.bh = x / p.n_qblk;
     u.qb = x - u.bh * p.n_qblk;
+    u.r0 = u.qb * 2 * kBM + half * kBM;
     return u;
   }
   const int per_group = p.group_heads * p.n_qblk;
@@ -211,6 +253,7 @@ __device__ __forceinline__ Unit decode_unit(int x, const FwdParams& p) {
   const int level = r / gh;
   u.bh = g * p.group_heads + (r - level * gh);
   u.qb = p.n_qblk - 1 - level;
+  u.r0 = u.qb * 2 * kBM;
   return u;
 }
 
@@ -420,13 +463,16 @@ __device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, flo
   return sum;
 }
 
-template <int D, int ET, bool CAUSAL>
+template <int D, int ET, bool CAUSAL, bool KSPLIT>
 __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using C = Cfg<D, ET>;
+  // KSPLIT: the grid's units from p.n_whole on are key-split (a separate
+  // instantiation, so that launches without them run none of its code)
+  static_assert(!KSPLIT || (C::kKeySplit && !CAUSAL), "key-split units: full attention, one issuer");
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need 1024-byte aligned tiles
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -461,6 +507,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       mbar_init(&ctl.o_full[t], 1);
       mbar_init(&ctl.o_empty[t], 4);
     }
+    mbar_init(&ctl.merge, 128);  // every thread of tile 1 (key-split instantiations)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl.kv_full[s], 1);
       mbar_init(&ctl.kv_empty[0][s], 1);
@@ -528,9 +575,13 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       }
       __syncwarp();
       if (x < 0) break;
-      const Unit u = decode_unit<CAUSAL>(x, p);
-      const int q0 = u.qb * 2 * kBM;
-      const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
+      const Unit u = decode_unit<CAUSAL, KSPLIT>(x, p);
+      const bool ks = KSPLIT && u.ks;
+      // key blocks per tile; a key-split unit loads K_j, K_{h+j}, V_j, V_{h+j}
+      // per step j (tile 0 reads key block j, tile 1 key block h + j)
+      const int nkv0 = ks ? nkv_all / 2 : nkv_tile0(u.qb);
+      const int nkv1 = ks ? nkv_all / 2 : nkv_tile1(u.qb);
+      const int per_step = ks ? 4 : 2;
       if (p.dynamic) {
         // ask for the next unit now; the answer is read half-way through this one
         fence_proxy_async_smem();
@@ -540,7 +591,9 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       }
       int x_next = -1;
       for (int j = 0; ok && j < nkv1; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
+        for (int e = 0; e < per_step; ++e) {
+          const int kv = ks ? e >> 1 : e;
+          const int kb = ks && (e & 1) ? nkv1 + j : j;  // key block
           const uint32_t slot = it % C::kStages, bit = 1u << slot;
           if (rd0 & bit)
             ok = mbar_wait(&ctl.kv_empty[0][slot], (par0 & bit) ? 0u : 1u, abort_flag, p.status,
@@ -563,18 +616,18 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
           mbar_arrive_expect_tx_warp(&ctl.kv_full[slot], C::kSlotBytes);
           if (ET == kE4M3 && kv) {
             // V transposed: one box of 128 keys x 128 rows (d)
-            tma_load_3d_warp(sRing + slot * C::kSlotBytes, &tm_v, &ctl.kv_full[slot], j * kBN, 0,
+            tma_load_3d_warp(sRing + slot * C::kSlotBytes, &tm_v, &ctl.kv_full[slot], kb * kBN, 0,
                              u.bh, pol_kv);
           } else {
             const CUtensorMap* m = kv ? &tm_v : &tm_k;
             for (int cb = 0; cb < C::kColBlocks; ++cb)
               tma_load_3d_warp(sRing + slot * C::kSlotBytes + cb * (kBN * 128), m,
-                               &ctl.kv_full[slot], cb * C::kBoxElems, j * kBN, u.bh, pol_kv);
+                               &ctl.kv_full[slot], cb * C::kBoxElems, kb * kBN, u.bh, pol_kv);
           }
           ++it;
-          if (j == 0 && kv == 1) {
-            // Q_t after K_0 and V_0: the previous unit's last Q_t K^T frees
-            // the tile while this unit's first K/V are already in flight.
+          if (j == 0 && e == per_step - 1) {
+            // Q_t after the first step's K and V: the previous unit's last
+            // Q_t K^T frees the tile while this unit's first K/V are in flight.
             for (int t = 0; ok && t < 2; ++t) {
               ok = mbar_wait(&ctl.q_empty[t], (nq[t] & 1) ^ 1, abort_flag, p.status,
                              kStatusTimeoutLoad, p.wait_limit_ns);
@@ -583,12 +636,12 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
               mbar_arrive_expect_tx_warp(&ctl.q_full[t], C::kTileBytes);
               for (int cb = 0; cb < C::kColBlocks; ++cb)
                 tma_load_3d_warp(sQ + t * C::kTileBytes + cb * (kBM * 128), &tm_q, &ctl.q_full[t],
-                                 cb * C::kBoxElems, q0 + t * kBM, u.bh, pol_q);
+                                 cb * C::kBoxElems, tile_row0<KSPLIT>(u, t), u.bh, pol_q);
               ++nq[t];
             }
             if (!ok) break;
           }
-          if (p.dynamic && j == nkv1 / 2 && kv == 1) {
+          if (p.dynamic && j == nkv1 / 2 && e == per_step - 1) {
             ok = mbar_wait(&ctl.clc_bar, answered & 1, abort_flag, p.status, kStatusTimeoutLoad,
                            p.wait_limit_ns);
             ok = __all_sync(0xffffffffu, ok);
@@ -597,10 +650,10 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
             ++answered;
             if (x_next >= 0) {
               // the next unit's Q into L2 while this unit still streams
-              const Unit un = decode_unit<CAUSAL>(x_next, p);
+              const Unit un = decode_unit<CAUSAL, KSPLIT>(x_next, p);
               for (int t = 0; t < 2; ++t)
                 for (int cb = 0; cb < C::kColBlocks; ++cb)
-                  tma_prefetch_3d_warp(&tm_q, cb * C::kBoxElems, un.qb * 2 * kBM + t * kBM, un.bh);
+                  tma_prefetch_3d_warp(&tm_q, cb * C::kBoxElems, tile_row0<KSPLIT>(un, t), un.bh);
             }
           }
         }
@@ -681,7 +734,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         int x;
         ok = next_unit(k, kStatusTimeoutMma, &x);
         if (!ok || x < 0) break;
-        const Unit u = decode_unit<CAUSAL>(x, p);
+        const Unit u = decode_unit<CAUSAL, KSPLIT>(x, p);
         const int nkv = t ? nkv_tile1(u.qb) : nkv_tile0(u.qb);
         const int nkv1 = nkv_tile1(u.qb);  // the unit's key blocks (ring items / 2)
         // S_t is overwritten only after the softmax has read it
@@ -722,11 +775,66 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         mma_commit_warp(&ctl.q_empty[1]);
       };
       uint32_t g0 = 0, g1 = 0;  // key blocks done by tile 0 / tile 1
+      // A key-split unit (h key blocks per tile): the same issue order, but
+      // each tile reads its own K and V -- ring items 4j + t and 4j + 2 + t of
+      // step j -- and each item is released after its tile's MMAs.  (Whole
+      // units keep their own loop below: this schedule's issue loop is the
+      // critical path, and folding both into one costs whole units 1-3 %.)
+      auto run_split_unit = [&](uint32_t k, int h) -> bool {
+        bool good = wait_full(it) && wait_full(it + 1) && wait(&ctl.q_full[0], k & 1) &&
+                    wait(&ctl.q_full[1], k & 1);
+        if (!good) return false;
+        tc_fence_after();
+        issue_qk<D, ET>(tS0, q0_lo, k_lo(it));
+        mma_commit_warp(&ctl.s_full[0]);
+        issue_qk<D, ET>(tS1, q1_lo, k_lo(it + 1));
+        mma_commit_warp(&ctl.s_full[1]);
+        release(it);
+        release(it + 1);
+        if (h == 1) free_q();
+        good = wait(&ctl.o_empty[0], (k & 1) ^ 1) && wait(&ctl.o_empty[1], (k & 1) ^ 1);
+        for (int j = 0; good && j < h; ++j) {
+          const uint32_t step = it + 4 * j;  // K_j, K_{h+j}, V_j, V_{h+j}
+          const bool more = j + 1 < h;
+          good = wait_full(step + 2) && pv_halves(0, tO0, tS0, v_lo(step + 2), g0 + j, j);
+          if (!good) break;
+          if (j == h - 1) mma_commit_warp(&ctl.o_full[0]);
+          release(step + 2);
+          if (more) {
+            if (!(good = wait_full(step + 4))) break;
+            tc_fence_after();
+            issue_qk<D, ET>(tS0, q0_lo, k_lo(step + 4));
+            mma_commit_warp(&ctl.s_full[0]);
+            release(step + 4);
+          }
+          good = wait_full(step + 3) && pv_halves(1, tO1, tS1, v_lo(step + 3), g1 + j, j);
+          if (!good) break;
+          release(step + 3);
+          if (j == h - 1) mma_commit_warp(&ctl.o_full[1]);
+          if (more) {
+            if (!(good = wait_full(step + 5))) break;
+            tc_fence_after();
+            issue_qk<D, ET>(tS1, q1_lo, k_lo(step + 5));
+            mma_commit_warp(&ctl.s_full[1]);
+            release(step + 5);
+            if (j + 2 == h) free_q();
+          }
+        }
+        return good;
+      };
       for (uint32_t k = 0; ok; ++k) {
         int x;
         ok = next_unit(k, kStatusTimeoutMma, &x);
         if (!ok || x < 0) break;
-        const Unit u = decode_unit<CAUSAL>(x, p);
+        const Unit u = decode_unit<CAUSAL, KSPLIT>(x, p);
+        if (KSPLIT && u.ks) {
+          const int h = nkv_all / 2;
+          ok = run_split_unit(k, h);
+          it += 4 * h;
+          g0 += h;
+          g1 += h;
+          continue;
+        }
         const int nkv0 = nkv_tile0(u.qb), nkv1 = nkv_tile1(u.qb);
         ok = wait_full(it) && wait(&ctl.q_full[0], k & 1) && wait(&ctl.q_full[1], k & 1);
         if (!ok) break;
@@ -794,11 +902,16 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       int x;
       ok = next_unit(k, kStatusTimeoutSoftmax, &x);
       if (!ok || x < 0) break;
-      const Unit u = decode_unit<CAUSAL>(x, p);
-      const int row = u.qb * 2 * kBM + t * kBM + quad * 32 + lane;
-      const int nkv = t ? nkv_tile1(u.qb) : nkv_tile0(u.qb);
-      // keys visible to this row: [0, lim)
-      const int lim = CAUSAL ? min(row + 1, S) : S;
+      const Unit u = decode_unit<CAUSAL, KSPLIT>(x, p);
+      const bool ks = KSPLIT && u.ks;
+      const int row = tile_row0<KSPLIT>(u, t) + quad * 32 + lane;
+      // key blocks of this tile: a key-split unit gives tile 0 the first half
+      // and tile 1 the second
+      const int nkv = ks ? nkv_all / 2 : (t ? nkv_tile1(u.qb) : nkv_tile0(u.qb));
+      // keys visible to this row, counted from the tile's first key block:
+      // [0, lim).  (Tile 0 of a key-split unit ends half-way through the keys;
+      // its last block goes through the masking path with nothing to mask.)
+      const int lim = (CAUSAL ? min(row + 1, S) : S) - (ks && t ? nkv * kBN : 0);
 
       float m = -INFINITY;  // running maximum, log2 units of the scaled logits
       float l = 0.f;        // running sum of exp2(s*c - m)
@@ -984,9 +1097,50 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
       }
       if (!ok) break;
+      // (key-split kernels decode the unit again: fewer values live across
+      // the block loop)
+      const Unit ue = KSPLIT ? decode_unit<CAUSAL, KSPLIT>(x, p) : u;
+      const bool kse = KSPLIT && ue.ks;
+      // tile 1's warp 4 + quad leaves its rows' statistics in its staging box
+      float2* const stat = reinterpret_cast<float2*>(
+          smem + C::kStageOff + (4 + quad) * (C::kStageBoxes * C::kStageBoxBytes));
+      if (KSPLIT && t == 1) {
+        // A key-split unit: hand this row's statistics to tile 0, which
+        // merges O_1 into its result and frees O_1.  Every thread of tile 1
+        // arrives in every unit, so phase k of the barrier is unit k's.
+        if (kse) {
+          if (lane == 0) bulk_wait_group_read<0>();  // the box's last store has read it
+          __syncwarp();
+          stat[lane] = make_float2(m, l);
+        }
+        mbar_arrive(&ctl.merge);
+        if (kse) continue;
+      }
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const int row0 = u.qb * 2 * kBM + t * kBM + quad * 32;  // the warp's first row
+      float inv_l = 1.f / l;
+      // Merging a key-split unit: with m = max(m_0, m_1) and
+      // l = l_0 2^(m_0 - m) + l_1 2^(m_1 - m), O = w0 O_0 + w1 O_1 where
+      // w_t = 2^(m_t - m) / l (then scaled by inv_l = 1).
+      float w0 = 0.f, w1 = 0.f;
+      if (kse) {
+        ok = mbar_wait(&ctl.o_full[1], k & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
+                       p.wait_limit_ns) &&
+             mbar_wait(&ctl.merge, k & 1, abort_flag, p.status, kStatusTimeoutSoftmax,
+                       p.wait_limit_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const float2 other = stat[lane];
+        const float mx = fmaxf(m, other.x);
+        const float a0 = ex2(m - mx), a1 = ex2(other.x - mx);
+        m = mx;
+        l = l * a0 + other.y * a1;
+        const float inv = 1.f / l;
+        w0 = a0 * inv;
+        w1 = a1 * inv;
+        inv_l = 1.f;
+      }
+      const int row0 = tile_row0<KSPLIT>(ue, t) + quad * 32;  // the warp's first row
       const uint32_t stage = sStage + warp * (C::kStageBoxes * C::kStageBoxBytes);
 #pragma unroll 1
       for (int cb = 0; cb < C::kOutColBlocks; ++cb) {
@@ -998,6 +1152,14 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           uint32_t orr[32];
           tmem_ld_x32(tO + cb * 64 + h * 32, orr);
+          if (kse) {
+            uint32_t o1[32];
+            tmem_ld_x32(lane_base + C::kOCol + D + cb * 64 + h * 32, o1);  // O_1
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              orr[i] = __float_as_uint(
+                  fmaf(__uint_as_float(o1[i]), w1, __uint_as_float(orr[i]) * w0));
+          }
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const int c = h * 4 + c4;
@@ -1012,16 +1174,20 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         fence_proxy_async_smem();  // this lane's writes, visible to the TMA engine
         __syncwarp();
         if (lane == 0) {
-          if (row0 < S) tma_store_3d(&tm_o, box, cb * 64, row0, u.bh);  // rows >= S clipped
+          if (row0 < S) tma_store_3d(&tm_o, box, cb * 64, row0, ue.bh);  // rows >= S clipped
           bulk_commit_group();
         }
       }
-      // O_t has left TMEM: the next unit's first P V may overwrite it
+      // O_t (and O_1 after a merge) has left TMEM: the next unit's first P V
+      // may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.o_empty[t]);
+      if (lane == 0) {
+        mbar_arrive(&ctl.o_empty[t]);
+        if (kse) mbar_arrive(&ctl.o_empty[1]);
+      }
       if (row < S)
-        p.lse[static_cast<size_t>(u.bh) * S + row] =
+        p.lse[static_cast<size_t>(ue.bh) * S + row] =
             (m + lg2(l) - shift) * 0.69314718055994530942f;
     }
     // every TMA store of O has completed before the block may exit
@@ -1042,11 +1208,11 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
 // linkage keeps the flags private to each loaded copy of the library (a
 // function-local static of an inline template would otherwise become one
 // process-wide symbol shared by every copy).
-template <int D, int ET, bool CAUSAL>
+template <int D, int ET, bool CAUSAL, bool KSPLIT = false>
 static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const FwdParams& prm, unsigned grid,
                             cudaStream_t stream) {
-  auto kern = fmha_fwd_kernel<D, ET, CAUSAL>;
+  auto kern = fmha_fwd_kernel<D, ET, CAUSAL, KSPLIT>;
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> opted_in[kMaxDevices];
   int dev = 0;

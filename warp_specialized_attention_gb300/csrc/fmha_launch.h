@@ -26,6 +26,12 @@ cudaError_t launch_fwd_e4m3(bool causal, const CUtensorMap& tq, const CUtensorMa
                             const CUtensorMap& tvt, const CUtensorMap& to, const FwdParams& prm,
                             unsigned grid, cudaStream_t stream);
 
+// Full attention, head dim 128, with the grid's units from prm.n_whole on
+// key-split; et = kF16, kBF16 or kE4M3 (the maps as for the launchers above).
+cudaError_t launch_fwd_ksplit(int et, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& prm,
+                              unsigned grid, cudaStream_t stream);
+
 // Backward pass (16-bit, D = 64 or 128): the main kernel over (head, key
 // block), the delta pre-pass over rows, and the dQ conversion of n elements.
 // tdq maps the fp32 dQ accumulator (D, S, B*H) with 16 x 32 x 1 boxes and the
