@@ -91,6 +91,10 @@
 #include "ptx.cuh"
 
 namespace wsa {
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
 
 constexpr int kBM = 128;       // query rows per tile (tcgen05 M)
 constexpr int kBN = 128;       // keys per block
@@ -507,7 +511,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       mbar_init(&ctl.o_full[t], 1);
       mbar_init(&ctl.o_empty[t], 4);
     }
-    mbar_init(&ctl.merge, 128);  // every thread of tile 1 (key-split instantiations)
+    mbar_init(&ctl.merge, 4);  // every warp of tile 1 (key-split instantiations)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&ctl.kv_full[s], 1);
       mbar_init(&ctl.kv_empty[0][s], 1);
@@ -1106,14 +1110,15 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
           smem + C::kStageOff + (4 + quad) * (C::kStageBoxes * C::kStageBoxBytes));
       if (KSPLIT && t == 1) {
         // A key-split unit: hand this row's statistics to tile 0, which
-        // merges O_1 into its result and frees O_1.  Every thread of tile 1
+        // merges O_1 into its result and frees O_1.  Every warp of tile 1
         // arrives in every unit, so phase k of the barrier is unit k's.
         if (kse) {
           if (lane == 0) bulk_wait_group_read<0>();  // the box's last store has read it
           __syncwarp();
           stat[lane] = make_float2(m, l);
         }
-        mbar_arrive(&ctl.merge);
+        __syncwarp();  // the warp's statistics, ordered before lane 0's arrival
+        if (lane == 0) mbar_arrive(&ctl.merge);
         if (kse) continue;
       }
       tc_fence_after();
@@ -1142,42 +1147,50 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       }
       const int row0 = tile_row0<KSPLIT>(ue, t) + quad * 32;  // the warp's first row
       const uint32_t stage = sStage + warp * (C::kStageBoxes * C::kStageBoxBytes);
+      // One pass over the 64-column blocks of O; MERGE adds w1 O_1 to w0 O_t.
+      auto store_o = [&](auto merge_tag) {
+        constexpr bool MERGE = decltype(merge_tag)::value;
 #pragma unroll 1
-      for (int cb = 0; cb < C::kOutColBlocks; ++cb) {
-        const uint32_t box = stage + (cb % C::kStageBoxes) * C::kStageBoxBytes;
-        // the box's previous TMA store has finished reading it
-        if (lane == 0) bulk_wait_group_read<C::kStageBoxes - 1>();
-        __syncwarp();
+        for (int cb = 0; cb < C::kOutColBlocks; ++cb) {
+          const uint32_t box = stage + (cb % C::kStageBoxes) * C::kStageBoxBytes;
+          // the box's previous TMA store has finished reading it
+          if (lane == 0) bulk_wait_group_read<C::kStageBoxes - 1>();
+          __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t orr[32];
-          tmem_ld_x32(tO + cb * 64 + h * 32, orr);
-          if (kse) {
-            uint32_t o1[32];
-            tmem_ld_x32(lane_base + C::kOCol + D + cb * 64 + h * 32, o1);  // O_1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t orr[32];
+            tmem_ld_x32(tO + cb * 64 + h * 32, orr);
+            if (MERGE) {
+              uint32_t o1[32];
+              tmem_ld_x32(lane_base + C::kOCol + D + cb * 64 + h * 32, o1);  // O_1
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orr[i] = __float_as_uint(
-                  fmaf(__uint_as_float(o1[i]), w1, __uint_as_float(orr[i]) * w0));
+              for (int i = 0; i < 32; ++i)
+                orr[i] = __float_as_uint(
+                    fmaf(__uint_as_float(o1[i]), w1, __uint_as_float(orr[i]) * w0));
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int c = h * 4 + c4;
+              uint32_t w4[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w4[i] = pack2<ET != kF16>(__uint_as_float(orr[c4 * 8 + 2 * i]) * inv_l,
+                                          __uint_as_float(orr[c4 * 8 + 2 * i + 1]) * inv_l);
+              st_shared_v4(box + lane * 128 + ((c ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+            }
           }
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const int c = h * 4 + c4;
-            uint32_t w4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              w4[i] = pack2<ET != kF16>(__uint_as_float(orr[c4 * 8 + 2 * i]) * inv_l,
-                                        __uint_as_float(orr[c4 * 8 + 2 * i + 1]) * inv_l);
-            st_shared_v4(box + lane * 128 + ((c ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+          fence_proxy_async_smem();  // this lane's writes, visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            if (row0 < S) tma_store_3d(&tm_o, box, cb * 64, row0, ue.bh);  // rows >= S clipped
+            bulk_commit_group();
           }
         }
-        fence_proxy_async_smem();  // this lane's writes, visible to the TMA engine
-        __syncwarp();
-        if (lane == 0) {
-          if (row0 < S) tma_store_3d(&tm_o, box, cb * 64, row0, ue.bh);  // rows >= S clipped
-          bulk_commit_group();
-        }
-      }
+      };
+      if (KSPLIT && kse)
+        store_o(BoolTag<KSPLIT>{});
+      else
+        store_o(BoolTag<false>{});
       // O_t (and O_1 after a merge) has left TMEM: the next unit's first P V
       // may overwrite it
       tc_fence_before();
