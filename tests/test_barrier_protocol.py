@@ -302,13 +302,11 @@ class Model:
                 yield from self.wait(("s_full", t), gj)
                 if self.split:
                     self.bars[("s_free", t)].arrive()
+                    # the previous block's whole P V (both halves, committed in
+                    # order) has read the P columns before any P is rewritten
                     if gj > 0:
-                        yield from self.wait(("pva", t), gj - 1)
-                    if j > 0 and rng.random() < 0.2:      # keys 0-63 raise the maximum
                         yield from self.wait(("pvb", t), gj - 1)
                     self.bars[("p0", t)].arrive()
-                    if gj > 0:
-                        yield from self.wait(("pvb", t), gj - 1)
                 else:
                     self.bars[("p0", t)].arrive()
                 for _ in range(rng.randint(0, 2)):

@@ -971,7 +971,14 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
             mask_keys<64, 64>(hi, lim_blk);
           }
           if (j == 0) m = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
-          if (gj > 0 && !wait_all(&ctl.pva_done[t], (gj - 1) & 1)) break;
+          // The previous block's P V has read both halves of the P columns
+          // (its halves are committed in order, so one wait covers both: each
+          // wait costs the softmax warp a few hundred cycles on a sub-partition
+          // shared with the other tile's softmax).
+          if (gj > 0) {
+            if (!wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
+            tc_fence_after();  // the P stores below follow the MMAs' reads
+          }
           float la = exp_keys_regs<ET>(lo, cl2, m - shift, tP, 0);
           // (the lazy-maximum test of the streaming path below, on registers)
           bool check = j > 0 && la > p.two_pow_tau;
@@ -979,9 +986,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
             const float bmax = row_max<64>(lo) * cl2;
             const bool raise = check && bmax > m + p.tau;
             if (__any_sync(0xffffffffu, raise)) {
-              // O_t must hold every earlier block before it is scaled
-              if (!wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
-              tc_fence_after();
+              // O_t holds every earlier block (waited above) before it is scaled
               const float alpha = raise ? ex2(m - bmax) : 1.f;
               if (raise) m = bmax;
               l *= alpha;
@@ -992,7 +997,6 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
           }
           l += la;
           release(0);
-          if (gj > 0 && !wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
           float lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
           check = j > 0 && lb > p.two_pow_tau;
           if (__any_sync(0xffffffffu, check)) {
