@@ -22,10 +22,11 @@ warp_specialized_attention_gb300/csrc/fmha_fwd_sm103.cuh:
   MMA        the head-dim 128 schedule (P over S): one issuer for both tiles
              in the order P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1), releasing
              every ring item and both Q tiles; the head-dim 64 one (split P:
-             s_free, pva_done/pvb_done): one issuer per query tile, each
-             releasing the ring items and the Q tile its tile read
-  softmax    4 warps per query tile: S wait, P releases in two halves, the
-             rescale waits, epilogue (o_full/o_empty); in a key-split unit
+             s_free, P handed over whole, pvb_done): one issuer per query
+             tile, each releasing the ring items and the Q tile its tile read
+  softmax    4 warps per query tile: S wait, P releases (in two halves over
+             S, whole with split P), the rescale waits, epilogue
+             (o_full/o_empty); in a key-split unit
              (both tiles on the same 128 query rows, tile 0 on the first half
              of the keys, tile 1 on the second) tile 1 hands its row
              statistics over (merge) and tile 0 writes the merged result and
@@ -191,11 +192,13 @@ class Model:
                     if j + 2 == n:
                         self.commit(t, ("q_empty", t))
                 yield from use(V(j))
-                yield from self.wait(("p0", t), g + j)
-                self.commit(t, ("pva", t))
-                yield from self.wait(("p1", t), g + j)
-                if self.split:
+                if self.split:                            # P handed over whole
+                    yield from self.wait(("p1", t), g + j)
                     self.commit(t, ("pvb", t))
+                else:
+                    yield from self.wait(("p0", t), g + j)
+                    self.commit(t, ("pva", t))
+                    yield from self.wait(("p1", t), g + j)
                 release(V(j))
                 if j == n - 1:
                     self.commit(t, ("o_full", t))
@@ -302,13 +305,16 @@ class Model:
                 yield from self.wait(("s_full", t), gj)
                 if self.split:
                     self.bars[("s_free", t)].arrive()
-                    # the previous block's whole P V (both halves, committed in
-                    # order) has read the P columns before any P is rewritten
+                    # the previous block's whole P V has read the P columns
+                    # before any P is rewritten; a raised maximum rescales
+                    # O_t, which holds exactly the earlier blocks then
                     if gj > 0:
                         yield from self.wait(("pvb", t), gj - 1)
-                    self.bars[("p0", t)].arrive()
-                else:
-                    self.bars[("p0", t)].arrive()
+                    for _ in range(rng.randint(0, 2)):
+                        yield
+                    self.bars[("p1", t)].arrive()        # all of P at once
+                    continue
+                self.bars[("p0", t)].arrive()
                 for _ in range(rng.randint(0, 2)):
                     yield
                 if j > 0 and rng.random() < 0.2:          # keys 64-127 raise the maximum

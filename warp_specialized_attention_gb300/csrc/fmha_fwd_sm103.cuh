@@ -64,7 +64,12 @@
 // warp once P_t of key half h -- keys 64h..64h+63 -- is in TMEM, so the MMA
 // multiplies the first half into O_t while the softmax computes the second),
 // pva_done[t] (commit after that first half, awaited only by a softmax that
-// must rescale O_t mid-block), o_full[t] (commit after the last P_t V).
+// must rescale O_t mid-block), o_full[t] (commit after the last P_t V).  With
+// split P (D = 64) P_t is handed over whole, on p_half[t][1] alone, and
+// pvb_done[t] (commit after its P V) tells the softmax when it may rewrite
+// the P columns: there each hand-off, vote and wait costs the softmax warp a
+// few hundred cycles on a sub-partition shared with the other tile's softmax,
+// and whole-block hand-offs measured 6 % faster than half-block ones.
 //
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
 // O_1 [256+D,256+2D).  At D = 128, P_t overwrites the first columns of S_t
@@ -701,11 +706,21 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
     auto release = [&](uint32_t item) {
       mma_commit_warp(&ctl.kv_empty[issuer][item % C::kStages]);
     };
-    // O_t += P_t V in two key halves, each as soon as its P is in TMEM; the
-    // first half's completion is committed for a softmax that has to rescale
-    // O_t while computing the second half.  gj = the tile's block count over
-    // all units of this block (P phases).
+    // O_t += P_t V.  P over S: in two key halves, each as soon as its P is in
+    // TMEM; the first half's completion is committed for a softmax that has to
+    // rescale O_t while computing the second half.  Split P: both halves once
+    // all of P is in TMEM.  gj = the tile's block count over all units of this
+    // block (P phases).
     auto pv_halves = [&](int t, uint32_t tO, uint32_t tP, uint32_t vlo, uint32_t gj, int j) {
+      if constexpr (C::kSplitP) {
+        // split P is handed over whole (p_half[t][1])
+        if (!wait(&ctl.p_half[t][1], gj & 1)) return false;
+        tc_fence_after();
+        issue_pv_half<D, ET>(tO, tP, vlo, 0, j > 0);
+        issue_pv_half<D, ET>(tO, tP, vlo, 1, true);
+        mma_commit_warp(&ctl.pvb_done[t]);
+        return true;
+      }
       if (!wait(&ctl.p_half[t][0], gj & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, ET>(tO, tP, vlo, 0, j > 0);
@@ -713,7 +728,6 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
       if (!wait(&ctl.p_half[t][1], gj & 1)) return false;
       tc_fence_after();
       issue_pv_half<D, ET>(tO, tP, vlo, 1, true);
-      if constexpr (C::kSplitP) mma_commit_warp(&ctl.pvb_done[t]);
       return true;
     };
     bool ok = true;
@@ -938,6 +952,14 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
           if (lane == 0 && !(p.inject == 1 && t == 0 && k == 0 && j == 0 && half == 0))
             mbar_arrive(&ctl.p_half[t][half]);
         };
+        // Split P: all of P at once, signalled on p_half[t][1] alone.
+        auto release_both = [&]() {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && !(p.inject == 1 && t == 0 && k == 0 && j == 0))
+            mbar_arrive(&ctl.p_half[t][1]);
+        };
         // O_t *= alpha for threads with alpha != 1 (all lanes take part).
         auto rescale_o = [&](float alpha) {
 #pragma unroll 1
@@ -959,8 +981,8 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
         };
         if constexpr (C::kSplitP) {
           // Split P: read all of S_t and hand its columns back to the MMA
-          // issuer at once; P_t goes to its own columns, each half once the
-          // previous block's P V has finished reading that half.
+          // issuer at once; P_t goes to its own columns once the previous
+          // block's P V has finished reading them.
           const uint32_t gj = g + j;
           load_s(tS, lo, hi);
           tc_fence_before();
@@ -979,43 +1001,30 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
             if (!wait_all(&ctl.pvb_done[t], (gj - 1) & 1)) break;
             tc_fence_after();  // the P stores below follow the MMAs' reads
           }
+          // Both key halves, then one lazy-maximum test for the block (the
+          // test of the streaming path below, on registers) and one hand-off
+          // of all of P: every vote and release costs the softmax warp a few
+          // hundred cycles here.
           float la = exp_keys_regs<ET>(lo, cl2, m - shift, tP, 0);
-          // (the lazy-maximum test of the streaming path below, on registers)
-          bool check = j > 0 && la > p.two_pow_tau;
+          float lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
+          const bool check = j > 0 && (la > p.two_pow_tau || lb > p.two_pow_tau);
           if (__any_sync(0xffffffffu, check)) {
-            const float bmax = row_max<64>(lo) * cl2;
+            const float bmax = fmaxf(row_max<64>(lo), row_max<64>(hi)) * cl2;
             const bool raise = check && bmax > m + p.tau;
             if (__any_sync(0xffffffffu, raise)) {
-              // O_t holds every earlier block (waited above) before it is scaled
+              // O_t holds every earlier block (waited above) and none of this
+              // one (its P is not handed over yet): scale it, redo the block
               const float alpha = raise ? ex2(m - bmax) : 1.f;
               if (raise) m = bmax;
               l *= alpha;
               tmem_st_wait();
               la = exp_keys_regs<ET>(lo, cl2, m - shift, tP, 0);
-              rescale_o(alpha);
-            }
-          }
-          l += la;
-          release(0);
-          float lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
-          check = j > 0 && lb > p.two_pow_tau;
-          if (__any_sync(0xffffffffu, check)) {
-            const float bmax = row_max<64>(hi) * cl2;
-            const bool raise = check && bmax > m + p.tau;
-            if (__any_sync(0xffffffffu, raise)) {
-              // keys 0-63 of this block are being multiplied into O_t
-              if (!wait_all(&ctl.pva_done[t], gj & 1)) break;
-              tc_fence_after();
-              const float alpha = raise ? ex2(m - bmax) : 1.f;
-              if (raise) m = bmax;
-              l *= alpha;
-              tmem_st_wait();
               lb = exp_keys_regs<ET>(hi, cl2, m - shift, tP, 1);
               rescale_o(alpha);
             }
           }
-          l += lb;
-          release(1);
+          l += la + lb;
+          release_both();
         } else if (j == 0) {
           // First block: no running maximum yet, so take the block maximum first.
           load_s(tS, lo, hi);
