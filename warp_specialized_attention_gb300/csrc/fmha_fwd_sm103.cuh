@@ -122,7 +122,7 @@ enum : int {
   kStatusTimeoutDrain = 8,
 };
 
-template <int D, int ET>
+template <int D, int ET, bool CAUSAL = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(ET != kE4M3 || D == 128, "E4M3 inputs: head dim 128");
@@ -153,7 +153,15 @@ struct Cfg {
   // anyway, and one issuer per tile keeps a wait on one tile from holding up
   // the other tile's MMAs.
   static constexpr int kIssuers = kSplitP ? 2 : 1;
-  static constexpr int kThreads = kIssuers == 2 ? 352 : 320;  // 11 or 10 warps
+  // Register split (causal, D = 64): 12 warps (three whole warpgroups)
+  // launched at 168 registers (64,512); the producer warpgroup (warps 8-11)
+  // gives up to 152 and the two softmax warpgroups take 176: 128 x 152 +
+  // 256 x 176 = 64,512, exactly the launch's registers.  Measured +4 to +7 %
+  // on causal D = 64 and -8 % on full attention, which keeps 11 warps.
+  static constexpr bool kRegSplit = kIssuers == 2 && CAUSAL;
+  static constexpr int kRegProducer = 152, kRegSoftmax = 176;
+  static_assert(!kRegSplit || 128 * kRegProducer + 256 * kRegSoftmax == 384 * 168, "register split");
+  static constexpr int kThreads = kRegSplit ? 384 : kIssuers == 2 ? 352 : 320;  // 12, 11 or 10 warps
   static constexpr int kUnitReaders = 8 + kIssuers;           // softmax warps + issuers
   // Key-split units (full attention, one issuer): both tiles take the same
   // 128 query rows, tile 0 the first half of the key blocks and tile 1 the
@@ -473,12 +481,12 @@ __device__ __forceinline__ float exp_keys_regs(const uint32_t* s, float cl2, flo
 }
 
 template <int D, int ET, bool CAUSAL, bool KSPLIT>
-__global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, ET, CAUSAL>::kThreads, 1)
     fmha_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
-  using C = Cfg<D, ET>;
+  using C = Cfg<D, ET, CAUSAL>;
   // KSPLIT: the grid's units from p.n_whole on are key-split (a separate
   // instantiation, so that launches without them run none of its code)
   static_assert(!KSPLIT || (C::kKeySplit && !CAUSAL), "key-split units: full attention, one issuer");
@@ -553,6 +561,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
   };
 
   if (warp == kWarpLoad) {
+    if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegProducer>();
     // ================================================================ TMA producer
     // The whole warp runs the loop; one elected lane issues each copy.
     prefetch_tmap(&tm_q);
@@ -683,6 +692,7 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
                 kStatusTimeoutDrain, p.wait_limit_ns);
     __syncwarp();
   } else if (warp == kWarpMma || (C::kIssuers == 2 && warp == kWarpMma1)) {
+    if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegProducer>();
     // ================================================================ MMA issuers
     // Each issuer warp runs its loop with warp-uniform operands; one elected
     // lane issues every tcgen05.mma and tcgen05.commit.  A commit tracks only
@@ -903,8 +913,13 @@ __global__ void __launch_bounds__(Cfg<D, ET>::kThreads, 1)
     mbar_wait(&ctl.mma_drain[issuer], 0, nullptr, p.status, kStatusTimeoutDrain,
               p.wait_limit_ns);
     __syncwarp();
+  } else if (C::kRegSplit && warp == 11) {
+    // the producer warpgroup's fourth warp: no role, but every warp of a
+    // warpgroup takes part in its register release
+    setmaxnreg_dec<C::kRegProducer>();
   } else {
     // ================================================================ softmax tile t
+    if constexpr (C::kRegSplit) setmaxnreg_inc<C::kRegSoftmax>();
     const int t = warp >> 2;
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
@@ -1246,11 +1261,11 @@ static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D, ET>::kSmemBytes);
+                             Cfg<D, ET, CAUSAL>::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, Cfg<D, ET>::kThreads, Cfg<D, ET>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
+  kern<<<grid, Cfg<D, ET, CAUSAL>::kThreads, Cfg<D, ET, CAUSAL>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
   return cudaGetLastError();
 }
 

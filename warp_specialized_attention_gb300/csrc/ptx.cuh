@@ -310,6 +310,18 @@ __device__ __forceinline__ void tma_prefetch_3d_warp(const CUtensorMap* map, int
       : "memory");
 }
 
+// ---------------------------------------------------------------- register split
+// setmaxnreg: every warp of a warpgroup executes it.  .dec returns registers
+// to the block's pool; .inc waits until the pool holds enough.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- cluster launch control
 // A running block asks the hardware to cancel the launch of a block of the same
 // grid that has not started yet and to hand over its index: dynamic persistent
