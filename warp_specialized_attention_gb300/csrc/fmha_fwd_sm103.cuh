@@ -14,12 +14,18 @@
 // Specialization for Tensor Core GPUs" rediscovers for Hopper and Blackwell
 // (Section 6.2, Figs. 7-8), built here on Tensor Memory instead of registers.
 //
-// Warp roles (320 threads, one CTA per SM):
+// Warp roles (one CTA per SM; 384 threads, except 352 for full attention at
+// head dim 64):
 //   warps 0-3  softmax + epilogue, query tile 0 (TMEM lanes 0-127)
 //   warps 4-7  softmax + epilogue, query tile 1
-//   warp  8    TMEM allocator and the tcgen05.mma issuer
+//   warp  8    TMEM allocator and the tcgen05.mma issuer (of tile 0 at D = 64)
 //   warp  9    TMA producer and scheduler: per work unit Q, then K_j / V_j
 //              through an SMEM ring
+//   warp  10   the tcgen05.mma issuer of tile 1 at D = 64, else idle
+//   warp  11   idle
+// The two idle warps complete the third warpgroup, so that warps 8-11 can hand
+// registers to the softmax warpgroups with setmaxnreg (the register split in
+// Cfg).
 // The variable-latency TMA loads sit on their own warp and nothing blocking
 // shares a warp with the MMA issuer (the warp-specialization rules of the Twill
 // page, "core method": variable-latency ops on a dedicated warp, no blocking
@@ -153,13 +159,18 @@ struct Cfg {
   // anyway, and one issuer per tile keeps a wait on one tile from holding up
   // the other tile's MMAs.
   static constexpr int kIssuers = kSplitP ? 2 : 1;
-  // Register split (causal, D = 64): 12 warps (three whole warpgroups)
-  // launched at 168 registers (64,512); the producer warpgroup (warps 8-11)
-  // gives up to 152 and the two softmax warpgroups take 176: 128 x 152 +
-  // 256 x 176 = 64,512, exactly the launch's registers.  Measured +4 to +7 %
-  // on causal D = 64 and -8 % on full attention, which keeps 11 warps.
-  static constexpr bool kRegSplit = kIssuers == 2 && CAUSAL;
-  static constexpr int kRegProducer = 152, kRegSoftmax = 176;
+  // Register split: 12 warps (three whole warpgroups) launched at 168
+  // registers (64,512 in all); the producer warpgroup (warps 8-11: the MMA
+  // issuer(s), the TMA warp and idle warps) lowers its limit and the two
+  // softmax warpgroups raise theirs by the same total, so the raise never
+  // waits on registers that are not there.  D = 128: 104 / 200 (128 x 104 +
+  // 256 x 200 = 64,512); measured +1 % (S16K), +6 % (E4M3), +7 % (S1K) and
+  // +10-12 % (causal S4K), while a 12-warp launch without the split is slower
+  // than 10 warps.  Causal D = 64: 152 / 176, +4 to +7 %; full attention at
+  // D = 64 lost 8 % with it and keeps 11 warps.
+  static constexpr bool kRegSplit = D == 128 || (kIssuers == 2 && CAUSAL);
+  static constexpr int kRegProducer = D == 128 ? 104 : 152;
+  static constexpr int kRegSoftmax = D == 128 ? 200 : 176;
   static_assert(!kRegSplit || 128 * kRegProducer + 256 * kRegSoftmax == 384 * 168, "register split");
   static constexpr int kThreads = kRegSplit ? 384 : kIssuers == 2 ? 352 : 320;  // 12, 11 or 10 warps
   static constexpr int kUnitReaders = 8 + kIssuers;           // softmax warps + issuers
@@ -913,8 +924,8 @@ __global__ void __launch_bounds__(Cfg<D, ET, CAUSAL>::kThreads, 1)
     mbar_wait(&ctl.mma_drain[issuer], 0, nullptr, p.status, kStatusTimeoutDrain,
               p.wait_limit_ns);
     __syncwarp();
-  } else if (C::kRegSplit && warp == 11) {
-    // the producer warpgroup's fourth warp: no role, but every warp of a
+  } else if (C::kRegSplit && (warp == 11 || (C::kIssuers == 1 && warp == 10))) {
+    // the producer warpgroup's warps without a role: every warp of a
     // warpgroup takes part in its register release
     setmaxnreg_dec<C::kRegProducer>();
   } else {
