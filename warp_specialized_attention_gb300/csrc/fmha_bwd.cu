@@ -31,6 +31,12 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              BwdCfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // The register split hands out exactly the registers the block is
+    // launched with: refuse a build that gave the kernel another count.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kBwdRegLaunch) return cudaErrorInvalidConfiguration;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   kern<<<grid, kBwdThreads, BwdCfg<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, prm);

@@ -65,7 +65,7 @@ __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint3
 
 // ============================================================================ the kernel
 //
-// Attention backward for one (head, 128-key block) per block of 576 threads:
+// Attention backward for one (head, 128-key block) per block of 640 threads:
 //   warps 0-7  dS / P: key row 32(w % 4) + lane, query columns 64(w / 4) ..
 //              +63 (two warps per SM sub-partition split the block's
 //              columns); read S^T and dP^T from TMEM, write P^T (16-bit) over
@@ -78,6 +78,7 @@ __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint3
 //              global memory (several key blocks add into one row)
 //   warp 16    TMEM allocation and the tcgen05.mma issuer
 //   warp 17    TMA producer: K, V once; Q, dO per query block; LSE and delta
+//   warps 18-19 idle (they complete the producer warpgroup for setmaxnreg)
 // Per query block the issuer runs S^T = K Q^T, dP^T = V dO^T, then (once P^T
 // and dS^T are in place) dV += P^T dO, dK += dS^T Q and dQ = dS K.  Each
 // half of the compute warps writes its P^T over S^T columns only it reads
@@ -89,7 +90,16 @@ __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint3
 // Section III-B/III-E); every wait is bounded and raises the abort flag.
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBwdThreads = 576;
+// 20 warps (five whole warpgroups; warps 18 and 19 idle) launched at 96
+// registers (61,440 in all).  Register split: the P/dS warpgroups raise their
+// limit to 128, the dQ warpgroups lower theirs to 80 and the producer
+// warpgroup (MMA, TMA, two idle warps) to 64: 256 x 128 + 256 x 80 + 128 x 64
+// = 61,440, exactly the launch's registers.
+constexpr int kBwdThreads = 640;
+constexpr int kBwdRegLaunch = 96, kBwdRegCompute = 128, kBwdRegDq = 80, kBwdRegProducer = 64;
+static_assert(256 * kBwdRegCompute + 256 * kBwdRegDq + 128 * kBwdRegProducer ==
+                  kBwdThreads * kBwdRegLaunch,
+              "register split");
 constexpr int kBwdComputeWarps = 8;  // warps 0-7
 constexpr int kBwdDqWarps = 8;       // warps 8-15
 constexpr int kBwdWarpMma = 16;
@@ -247,6 +257,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kBwdWarpLoad) {
     // ================================================================ TMA producer
+    setmaxnreg_dec<kBwdRegProducer>();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
@@ -302,6 +313,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp == kBwdWarpMma) {
     // ================================================================ MMA issuer
+    setmaxnreg_dec<kBwdRegProducer>();
     const uint32_t k_lo = sdesc_lo(sK, kLboKMajor), v_lo = sdesc_lo(sV, kLboKMajor);
     const uint32_t do_lo = sdesc_lo(sDO, kLboKMajor);
     const uint32_t k_mn = sdesc_lo(sK, kLboV);
@@ -340,6 +352,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   } else if (warp < kBwdComputeWarps) {
     // ================================================================ P and dS (key rows)
+    setmaxnreg_inc<kBwdRegCompute>();
     const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
     const int r = quad * 32 + lane;               // key row in the block, TMEM lane
     const int key = kb * 128 + r;
@@ -501,6 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp < kBwdComputeWarps + kBwdDqWarps) {
     // ================================================================ dQ (query rows)
+    setmaxnreg_dec<kBwdRegDq>();
     constexpr int kCols = D / 2;  // columns of this warp
     const int quad = warp & 3, hc = (warp - kBwdComputeWarps) >> 2;
     const uint32_t t_dq = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kColDQ + hc * kCols;
@@ -548,6 +562,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (lane == 0) bulk_wait_group0();  // every reduction has landed
     __syncwarp();
+  } else {
+    // warps 18 and 19: no role, but every warp of the producer warpgroup takes
+    // part in its register release
+    setmaxnreg_dec<kBwdRegProducer>();
   }
 
   // ---- teardown: every role has drained its asynchronous work

@@ -128,6 +128,10 @@ enum : int {
   kStatusTimeoutDrain = 8,
 };
 
+// Registers per thread that a 12-warp block is launched with (65,536 / 384,
+// rounded down to the allocation granularity of 8).
+constexpr int kRegLaunch = 168;
+
 template <int D, int ET, bool CAUSAL = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
@@ -171,7 +175,8 @@ struct Cfg {
   static constexpr bool kRegSplit = D == 128 || (kIssuers == 2 && CAUSAL);
   static constexpr int kRegProducer = D == 128 ? 104 : 152;
   static constexpr int kRegSoftmax = D == 128 ? 200 : 176;
-  static_assert(!kRegSplit || 128 * kRegProducer + 256 * kRegSoftmax == 384 * 168, "register split");
+  static_assert(!kRegSplit || 128 * kRegProducer + 256 * kRegSoftmax == 384 * kRegLaunch,
+                "register split");
   static constexpr int kThreads = kRegSplit ? 384 : kIssuers == 2 ? 352 : 320;  // 12, 11 or 10 warps
   static constexpr int kUnitReaders = 8 + kIssuers;           // softmax warps + issuers
   // Key-split units (full attention, one issuer): both tiles take the same
@@ -1274,6 +1279,15 @@ static cudaError_t launch_fmha_fwd(const CUtensorMap& tq, const CUtensorMap& tk,
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<D, ET, CAUSAL>::kSmemBytes);
     if (e != cudaSuccess) return e;
+    // The register split hands out exactly the registers the block is
+    // launched with; a build that gave the kernel another count would leave
+    // setmaxnreg.inc waiting for registers that do not exist, so refuse it.
+    if (Cfg<D, ET, CAUSAL>::kRegSplit) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kRegLaunch) return cudaErrorInvalidConfiguration;
+    }
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
   kern<<<grid, Cfg<D, ET, CAUSAL>::kThreads, Cfg<D, ET, CAUSAL>::kSmemBytes, stream>>>(tq, tk, tv, to, prm);
