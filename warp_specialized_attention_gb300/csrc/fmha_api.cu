@@ -304,7 +304,11 @@ fmha_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
       : e4m3          ? wsa::launch_fwd_e4m3(causal != 0, tq, tk, tv, to, prm, grid, st)
       : D == 64       ? wsa::launch_fwd_d64(bf16, causal != 0, tq, tk, tv, to, prm, grid, st)
                       : wsa::launch_fwd_d128(bf16, causal != 0, tq, tk, tv, to, prm, grid, st);
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (e != cudaSuccess)
+    return cuda_fail(e, e == cudaErrorInvalidConfiguration
+                            ? "kernel launch (refused: the kernel's register count differs from "
+                              "the one its register split assumes)"
+                            : "kernel launch");
   return FMHA_OK;
 }
 
@@ -395,7 +399,10 @@ fmha_status bwd_enqueue(const void* q, const void* k, const void* v, const void*
   prm.wait_limit_ns = wait_limit_ns;
   if ((e = wsa::launch_bwd(static_cast<int>(D), bf16, causal != 0, tq, tk, tv, tdo, tdq, prm,
                            static_cast<unsigned>(n_blk * BH), st)) != cudaSuccess)
-    return cuda_fail(e, "backward kernel launch");
+    return cuda_fail(e, e == cudaErrorInvalidConfiguration
+                            ? "backward kernel launch (refused: the kernel's register count "
+                              "differs from the one its register split assumes)"
+                            : "backward kernel launch");
   if ((e = wsa::launch_bwd_dq(bf16, dq_acc, dq, BH * S * D, st)) != cudaSuccess)
     return cuda_fail(e, "dQ conversion launch");
   return FMHA_OK;
