@@ -68,6 +68,15 @@ fmha_status fmha_fwd_split_testing(const void* q, const void* k, const void* v, 
                                    int causal, float scale, fmha_dtype dtype, void* stream,
                                    int64_t split_units);
 
+/*
+ * fmha_fwd_split_policy -- how many of the last units fmha_fwd key-splits for
+ * this shape on a GPU with n_sm multiprocessors (host arithmetic only; no
+ * CUDA call).  Returns 0 where no unit is split (causal, D != 128, an odd
+ * ceil(S / 128), or a last wave of more than n_sm / 2 units), and -1 for
+ * sizes fmha_fwd would reject or n_sm < 1.
+ */
+int64_t fmha_fwd_split_policy(int64_t B, int64_t H, int64_t S, int64_t D, int causal, int n_sm);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,6 +166,27 @@ def test_split_hook_rejects_unsupported_splits(lib):
                                       -1) == wsa.FMHA_ERR_INVALID_ARG
 
 
+def test_split_policy(lib):
+    """The host's choice of key-split tail units: the remainder of the last
+    wave, when it fits in half of the multiprocessors."""
+    lib.fmha_fwd_split_policy.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int]
+    lib.fmha_fwd_split_policy.restype = ctypes.c_int64
+    pol = lib.fmha_fwd_split_policy
+    assert pol(4, 32, 1024, 128, 0, 152) == 56      # 512 units: 3 waves + 56
+    assert pol(1, 32, 4096, 128, 0, 152) == 56      # 512 units
+    assert pol(4, 32, 16384, 128, 0, 152) == 0      # 8192 units: remainder 136 > 76
+    assert pol(2, 16, 2048, 128, 0, 152) == 0       # 256 units: remainder 104 > 76
+    assert pol(1, 2, 1024, 128, 0, 152) == 8        # fewer units than SMs: all split
+    assert pol(1, 32, 16384, 128, 0, 152) == 72     # 2048 units: remainder 72
+    assert pol(4, 32, 1024, 128, 1, 152) == 0       # causal: longest-first order instead
+    assert pol(4, 32, 1024, 64, 0, 152) == 0        # head dim 64: one issuer per tile
+    assert pol(1, 1, 1152, 128, 0, 152) == 0        # 9 key blocks: odd
+    assert pol(1, 1, 128, 128, 0, 152) == 0         # a single key block
+    assert pol(4, 32, 1024, 128, 0, 148) == 68      # the count follows the SM count
+    assert pol(4, 32, 1024, 128, 0, 0) == -1
+    assert pol(0, 32, 1024, 128, 0, 152) == -1
+
+
 def test_e4m3_overlap_uses_the_byte_sizes(lib):
     """Inputs are 1 byte per element and O 2 bytes: an O that starts inside
     the second half of a same-count 16-bit-sized region of q is still past q's

@@ -684,6 +684,11 @@ fmha_status fmha_fwd_testing(const void* q, const void* k, const void* v, void* 
                   inject_fault, static_cast<uint64_t>(wait_limit_s * 1e9), tau);
 }
 
+int64_t fmha_fwd_split_policy(int64_t B, int64_t H, int64_t S, int64_t D, int causal, int n_sm) {
+  if (n_sm < 1 || validate_sizes(B, H, S, D, 1.f, FMHA_F16) != FMHA_OK) return -1;
+  return auto_split_units(((S + 255) / 256) * B * H, S, D, causal, n_sm);
+}
+
 fmha_status fmha_fwd_split_testing(const void* q, const void* k, const void* v, void* o,
                                    float* lse, int64_t B, int64_t H, int64_t S, int64_t D,
                                    int causal, float scale, fmha_dtype dtype, void* stream,
