@@ -19,6 +19,7 @@ import torch
 import oracle
 import synthetic
 import warp_specialized_attention_gb300 as wsa
+from test_parity import stratified_rows
 from test_parity_fp8 import _check as _check_e4m3
 
 pytestmark = pytest.mark.gpu
@@ -104,3 +105,28 @@ def test_key_split_e4m3(S, splits):
         _check_e4m3(o.cpu().double().numpy(), lse.cpu().double().numpy(), q, k, v,
                     [((0, h), rows) for h in range(2)], False, w.scale,
                     "%s split_units=%d" % (w.describe(), n))
+
+
+def test_headline_shape_at_batch_one_with_key_split_tail():
+    """B1 H32 S16384 D128 f16 through fmha_fwd: 2048 units leave a last wave of
+    72 on 152 SMs, so the tail runs as 144 key-split half-units, 64 key blocks
+    per tile.  Rows i = 0 (mod 8) plus the last 128 of all 32 slices against the
+    oracle -- every unit contributes rows, the split ones included."""
+    w = synthetic.Workload("headline-b1", 1, 32, 16384, 128, "f16", False, 1.0, 9501)
+    q, k, v = synthetic.make_inputs(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = _run(qd, kd, vd, w.scale, -1, qd.dtype)
+    o, lse = o.cpu(), lse.cpu()
+    rows = stratified_rows(w.S)
+    worst_o = worst_l = 0.0
+    for h in range(w.H):
+        o_ref, lse_ref = oracle.attention_rows(
+            q[0, h, rows].double().numpy(), k[0, h].double().numpy(),
+            v[0, h].double().numpy(), rows, False, w.scale)
+        og, lg = o[0, h, rows].double().numpy(), lse[0, h, rows].double().numpy()
+        assert np.isfinite(og).all() and np.isfinite(lg).all(), "non-finite output"
+        worst_o = max(worst_o, float(np.abs(og - o_ref).max()))
+        worst_l = max(worst_l, float(np.abs(lg - lse_ref).max()))
+    print("PARITY-SPLIT %s (%d rows x %d slices) max_err_O %.3e max_err_LSE %.3e"
+          % (w.describe(), rows.size, w.H, worst_o, worst_l))
+    assert worst_o <= TOL_O and worst_l <= TOL_LSE, "max err O %g LSE %g" % (worst_o, worst_l)
